@@ -1,0 +1,121 @@
+"""Logical model of one layer's sink + short-window KV cache (oracle side).
+
+Restates LongLive summary page (yunpan.plus), 方法 §3 高效长推理:
+* 帧汇聚点 (frame sink): the video's first frame chunk is pinned as global sink
+  tokens that stay in the KV cache for good and are concatenated with the keys
+  and values of every attention layer;
+* 短窗口注意力 (short-window attention): attention is limited to a fixed window of
+  recent frames, so the per-layer cache size depends on the window only.
+The LONGLIVE news page (paooo.com), LONGLIVE的技术原理, states the same pair.
+
+Readings (the pages leave them open):
+* region 0 holds the sink chunk (chunk 0); chunk c >= 1 lives in ring slot
+  (c-1) mod W, i.e. region 1 + (c-1) mod W, rows [region*Tc, (region+1)*Tc);
+* the window's W slots include the chunk currently being generated, so the
+  visible set of chunk c is {0} U {max(1, c-W+1) .. c};
+* a chunk is appended only when its slot is empty or already holds it
+  (re-appending the newest chunk overwrites it: one call per denoise step);
+  the caller evicts the oldest window chunk first; the sink is never evicted.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+class CacheStateError(Exception):
+    """The call is not valid in the cache's current state."""
+
+
+def region_of_chunk(c: int, window_chunks: int) -> int:
+    return 0 if c == 0 else 1 + (c - 1) % window_chunks
+
+
+def visible_chunks_of_step(c: int, window_chunks: int) -> list[int]:
+    """Chunks a query chunk c attends to, in logical order (sink first)."""
+    if c == 0:
+        return [0]
+    return [0] + list(range(max(1, c - window_chunks + 1), c + 1))
+
+
+class CacheModel:
+    """Dict-of-chunks model with the physical layout the library must produce."""
+
+    def __init__(self, heads: int, head_dim: int, chunk_tokens: int, window_chunks: int):
+        self.H, self.D, self.Tc, self.W = heads, head_dim, chunk_tokens, window_chunks
+        self.chunk_of_region = [-1] * (1 + window_chunks)
+        self.k: dict[int, np.ndarray] = {}
+        self.v: dict[int, np.ndarray] = {}
+
+    # -- state queries ------------------------------------------------------
+    def present_chunks(self) -> list[int]:
+        """Chunks in the cache in logical order: sink first, then oldest -> newest."""
+        win = sorted(c for c in self.chunk_of_region[1:] if c >= 0)
+        return ([0] if self.chunk_of_region[0] == 0 else []) + win
+
+    def newest(self) -> int:
+        p = self.present_chunks()
+        return p[-1] if p else -1
+
+    def kv_length(self) -> int:
+        return len(self.present_chunks()) * self.Tc
+
+    # -- state transitions --------------------------------------------------
+    def append(self, c: int, k: np.ndarray, v: np.ndarray) -> None:
+        if c < 0:
+            raise ValueError("negative chunk index")
+        if k.shape != (self.Tc, self.H, self.D) or v.shape != k.shape:
+            raise ValueError("chunk shape mismatch")
+        if self.chunk_of_region[0] != 0:
+            if c != 0:
+                raise CacheStateError("the sink (chunk 0) must be appended first")
+        else:
+            nw = self.newest()
+            if c not in (nw, nw + 1):
+                raise CacheStateError("only the newest chunk or the next one may be appended")
+        r = region_of_chunk(c, self.W)
+        if self.chunk_of_region[r] not in (-1, c):
+            raise CacheStateError("slot still holds an older chunk: evict it first")
+        self.chunk_of_region[r] = c
+        self.k[c] = np.array(k, dtype=np.float64, copy=True)
+        self.v[c] = np.array(v, dtype=np.float64, copy=True)
+
+    def evict(self, c: int) -> None:
+        if c == 0:
+            raise CacheStateError("the sink chunk is never evicted")
+        win = [x for x in self.present_chunks() if x != 0]
+        if c not in win:
+            raise CacheStateError("chunk is not in the window")
+        if c != win[0]:
+            raise CacheStateError("only the oldest window chunk may be evicted")
+        self.chunk_of_region[region_of_chunk(c, self.W)] = -1
+        del self.k[c], self.v[c]
+
+    def recache(self, chunk_ids: list[int], k_new: np.ndarray, v_new: np.ndarray) -> None:
+        """Overwrite the K/V of every present chunk (chunk_ids in logical order)."""
+        if list(chunk_ids) != self.present_chunks():
+            raise CacheStateError("recache must list exactly the cached chunks, sink first")
+        for i, c in enumerate(chunk_ids):
+            sl = slice(i * self.Tc, (i + 1) * self.Tc)
+            self.k[c] = np.array(k_new[sl], dtype=np.float64, copy=True)
+            self.v[c] = np.array(v_new[sl], dtype=np.float64, copy=True)
+
+    # -- views ---------------------------------------------------------------
+    def visible_kv(self):
+        """Visible K and V concatenated in logical order, [L][H][D]."""
+        cs = self.present_chunks()
+        if not cs or cs[0] != 0:
+            raise CacheStateError("attention needs the sink chunk")
+        return (np.concatenate([self.k[c] for c in cs], axis=0),
+                np.concatenate([self.v[c] for c in cs], axis=0))
+
+    def physical(self, fill=np.nan):
+        """Expected physical cache K, V [(1+W)*Tc][H][D]; empty regions hold ``fill``."""
+        rows = (1 + self.W) * self.Tc
+        K = np.full((rows, self.H, self.D), fill, dtype=np.float64)
+        V = np.full_like(K, fill)
+        for r, c in enumerate(self.chunk_of_region):
+            if c >= 0:
+                K[r * self.Tc:(r + 1) * self.Tc] = self.k[c]
+                V[r * self.Tc:(r + 1) * self.Tc] = self.v[c]
+        return K, V

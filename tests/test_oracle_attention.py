@@ -1,0 +1,220 @@
+"""Pins for the attention oracle and the cache model (CPU only).
+
+Brute-force pure-Python loops on the small case, a full block-causal masked
+softmax over the whole sequence (a different formulation) when the window
+covers every chunk, closed forms (one key, Q = 0), and the invariants the
+frame-sink / short-window description fixes.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention as oatt
+from oracle.cache_model import (CacheModel, CacheStateError, region_of_chunk,
+                                visible_chunks_of_step)
+from synth import TINY, LAYER_1P3B, bf16_to_f64, chunk_qkv
+
+
+def _brute_attention(q, k, v, scale):
+    """Pure-Python loops: q [Tq][H][D], k, v [L][H][D] nested lists/arrays."""
+    Tq, H, D = len(q), len(q[0]), len(q[0][0])
+    L = len(k)
+    out = [[[0.0] * D for _ in range(H)] for _ in range(Tq)]
+    for h in range(H):
+        for i in range(Tq):
+            logits = []
+            for j in range(L):
+                acc = 0.0
+                for d in range(D):
+                    acc += float(q[i][h][d]) * float(k[j][h][d])
+                logits.append(acc * scale)
+            m = max(logits)
+            w = [math.exp(x - m) for x in logits]
+            z = sum(w)
+            for d in range(D):
+                acc = 0.0
+                for j in range(L):
+                    acc += w[j] * float(v[j][h][d])
+                out[i][h][d] = acc / z
+    return np.array(out)
+
+
+def _stream_tiny(n_chunks=6, W=TINY.window_chunks, dist="rms1"):
+    sh = TINY
+    m = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, W)
+    steps = []
+    for c in range(n_chunks):
+        q, k, v = chunk_qkv(sh, 0, 0, c, dist)
+        if c > W:
+            m.evict(c - W)
+        m.append(c, bf16_to_f64(k), bf16_to_f64(v))
+        steps.append((c, bf16_to_f64(q), m.present_chunks(), *m.visible_kv()))
+    return steps
+
+
+def test_brute_force_tiny_stream():
+    scale = 1.0 / math.sqrt(TINY.head_dim)
+    sh = TINY
+    m = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    for c in range(6):
+        q, k, v = (bf16_to_f64(t) for t in chunk_qkv(sh, 0, 0, c, "rms1"))
+        if c > sh.window_chunks:
+            m.evict(c - sh.window_chunks)
+        m.append(c, k, v)
+        got = oatt.sinkwin_attention(m, q, scale)
+        kk, vv = m.visible_kv()
+        rows = [0, 7, 31] if c != 3 else list(range(32))
+        want = _brute_attention(q[rows], kk, vv, scale)
+        assert np.allclose(got[rows], want, rtol=0, atol=1e-12)
+
+
+def _block_causal_full(q_all, k_all, v_all, Tc, scale):
+    """Masked softmax over the whole concatenated sequence: query token i may see
+    key token j iff chunk(j) <= chunk(i)."""
+    T, H, D = q_all.shape
+    ci = np.arange(T) // Tc
+    mask = ci[None, :] <= ci[:, None]
+    out = np.empty_like(q_all)
+    for h in range(H):
+        s = (q_all[:, h, :] @ k_all[:, h, :].T) * scale
+        s = np.where(mask, s, -np.inf)
+        s -= s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ v_all[:, h, :]
+    return out
+
+
+def test_window_covering_all_chunks_equals_block_causal():
+    n = 5
+    sh = TINY
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    m = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, window_chunks=n)  # W >= all
+    qs, ks, vs, outs = [], [], [], []
+    for c in range(n):
+        q, k, v = (bf16_to_f64(t) for t in chunk_qkv(sh, 0, 0, c, "rms1"))
+        m.append(c, k, v)
+        qs.append(q), ks.append(k), vs.append(v)
+        outs.append(oatt.sinkwin_attention(m, q, scale))
+    full = _block_causal_full(np.concatenate(qs), np.concatenate(ks), np.concatenate(vs),
+                              sh.chunk_tokens, scale)
+    assert np.allclose(np.concatenate(outs), full, rtol=0, atol=1e-12)
+
+
+def test_probabilities_sum_to_one():
+    for c, q, _, k, v in _stream_tiny():
+        p = oatt.attention_probs(q, k, 0.125)
+        assert np.allclose(p.sum(axis=2), 1.0, atol=1e-12)
+        assert np.all(p >= 0)
+
+
+def test_single_key_returns_v_and_zero_query_returns_mean():
+    rng = np.random.default_rng(0)
+    k = rng.standard_normal((1, 2, 16))
+    v = rng.standard_normal((1, 2, 16))
+    q = rng.standard_normal((5, 2, 16))
+    assert np.allclose(oatt.attention(q, k, v, 0.3), np.broadcast_to(v, (5, 2, 16)), atol=0)
+    k = rng.standard_normal((40, 2, 16))
+    v = rng.standard_normal((40, 2, 16))
+    o = oatt.attention(np.zeros((3, 2, 16)), k, v, 0.3)
+    assert np.allclose(o, np.broadcast_to(v.mean(axis=0), (3, 2, 16)), atol=1e-14)
+
+
+def test_key_permutation_invariance():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((9, 3, 32))
+    k = rng.standard_normal((50, 3, 32))
+    v = rng.standard_normal((50, 3, 32))
+    perm = rng.permutation(50)
+    a = oatt.attention(q, k, v, 0.2)
+    b = oatt.attention(q, k[perm], v[perm], 0.2)
+    assert np.allclose(a, b, atol=1e-13)
+
+
+def test_evicted_chunk_has_no_influence_and_sink_always_does():
+    sh = TINY
+    W = sh.window_chunks
+    scale = 0.125
+    base = _stream_tiny()
+    for c, q, present, k, v in base:
+        assert present[0] == 0  # the sink is always there
+        assert present == visible_chunks_of_step(c, W)
+    # perturb an evicted chunk (chunk 1 is gone from step W+1 on): outputs identical
+    m1 = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, W)
+    m2 = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, W)
+    m3 = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, W)
+    for c in range(6):
+        q, k, v = (bf16_to_f64(t) for t in chunk_qkv(sh, 0, 0, c, "rms1"))
+        if c > W:
+            for mm in (m1, m2, m3):
+                mm.evict(c - W)
+        k2, v2 = (k + 3.0, v - 2.0) if c == 1 else (k, v)
+        k3, v3 = (k * 0.5 + 1.0, v + 1.0) if c == 0 else (k, v)
+        m1.append(c, k, v), m2.append(c, k2, v2), m3.append(c, k3, v3)
+        o1 = oatt.sinkwin_attention(m1, q, scale)
+        o2 = oatt.sinkwin_attention(m2, q, scale)
+        o3 = oatt.sinkwin_attention(m3, q, scale)
+        if 1 not in m1.present_chunks():
+            assert np.array_equal(o1, o2)  # bit-identical
+        else:
+            assert not np.allclose(o1, o2)
+        assert np.max(np.abs(o1 - o3)) > 1e-3  # the sink changes every step
+
+
+@pytest.mark.parametrize("sh,want", [
+    (TINY, [32, 64, 96, 96, 96, 96]),
+    (LAYER_1P3B, [4680, 9360, 14040, 18720, 18720, 18720]),
+])
+def test_kv_length_table(sh, want):
+    m = CacheModel(1, 16, sh.chunk_tokens, sh.window_chunks)
+    got = []
+    z = np.zeros((sh.chunk_tokens, 1, 16))
+    for c in range(6):
+        if c > sh.window_chunks:
+            m.evict(c - sh.window_chunks)
+        m.append(c, z, z)
+        got.append(m.kv_length())
+    assert got == want
+
+
+def test_slot_rule_and_physical_layout():
+    W, Tc = 3, 4
+    assert [region_of_chunk(c, W) for c in range(9)] == [0, 1, 2, 3, 1, 2, 3, 1, 2]
+    m = CacheModel(1, 16, Tc, W)
+    for c in range(7):
+        if c > W:
+            m.evict(c - W)
+        m.append(c, np.full((Tc, 1, 16), float(c)), np.full((Tc, 1, 16), -float(c)))
+    assert m.chunk_of_region == [0, 4, 5, 6]
+    K, V = m.physical()
+    assert np.array_equal(K[:, 0, 0], np.repeat([0.0, 4.0, 5.0, 6.0], Tc))
+    assert np.array_equal(V[:, 0, 0], -np.repeat([0.0, 4.0, 5.0, 6.0], Tc))
+
+
+def test_state_errors():
+    m = CacheModel(1, 16, 2, 2)
+    z = np.zeros((2, 1, 16))
+    with pytest.raises(CacheStateError):
+        m.append(1, z, z)  # sink first
+    m.append(0, z, z)
+    m.append(0, z, z)  # re-append newest: overwrite
+    with pytest.raises(CacheStateError):
+        m.append(2, z, z)  # skips chunk 1
+    m.append(1, z, z)
+    m.append(2, z, z)
+    with pytest.raises(CacheStateError):
+        m.append(3, z, z)  # slot of chunk 1 still occupied
+    with pytest.raises(CacheStateError):
+        m.evict(0)  # sink
+    with pytest.raises(CacheStateError):
+        m.evict(2)  # not the oldest
+    m.evict(1)
+    with pytest.raises(CacheStateError):
+        m.evict(1)
+    m.append(3, z, z)
+    with pytest.raises(CacheStateError):
+        m.recache([0, 3, 2], np.zeros((6, 1, 16)), np.zeros((6, 1, 16)))
+    m.recache([0, 2, 3], np.ones((6, 1, 16)), np.ones((6, 1, 16)))
+    assert m.k[3][0, 0, 0] == 1.0
