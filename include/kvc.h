@@ -1,0 +1,178 @@
+/*
+ * kvc.h -- C ABI of the sink + short-window KV-cache attention library (sm_103a).
+ *
+ * What it computes.  LongLive's frame-level autoregressive video generator keeps,
+ * per self-attention layer, a KV cache made of the first frame chunk pinned as
+ * "frame sink" tokens plus a short rolling window of recent chunks; each new
+ * chunk's queries attend to [sink | window] (LongLive summary page, yunpan.plus,
+ * 方法 §3 高效长推理: 短窗口注意力 and 帧汇聚点; LONGLIVE news page, paooo.com,
+ * LONGLIVE的技术原理).  At a prompt switch the cache is rebuilt from the frames
+ * already generated (方法 §1 KV 重缓存).  LongLive 2.0 can hold the cache in FP4
+ * and dequantise it inside the attention read (LongLive 2.0 inference blog,
+ * blog.hotdry.top, "NVFP4 量化与 KV Cache 压缩的工程实现": inference.kv_quant).
+ *
+ * Layout.  One layer's cache has (1 + W) regions of Tc = chunk_frames *
+ * tokens_per_frame rows each.  Region 0 holds the sink (chunk 0); chunk c >= 1
+ * lives in region 1 + (c - 1) % W.  Row r of region g is physical row
+ * g * Tc + r of
+ *     bf16 cache:  k, v            bf16  [S][H][D]          S = (1 + W) * Tc
+ *     FP4 cache:   k, v            uint8 [S][H][D/2]        E2M1 codes, element 2i in
+ *                                                           the low nibble
+ *                  k_scale,v_scale uint8 [S][H][D/16]       E4M3 scale per 16 elements
+ *                  k_gscale,...    float [1 + W]            fp32 tensor scale per region
+ * Decoded value: e2m1(code) * e4m3(scale) * gscale[region].
+ *
+ * Conventions.
+ *  - All device memory (cache, inputs, outputs, workspace) is allocated by the
+ *    caller; the library allocates nothing and frees nothing.  The kvc_cache
+ *    struct is caller-owned host memory.
+ *  - Pointers documented as "device" are CUDA device addresses; "host" ones are
+ *    ordinary host addresses.  Device buffers must be 16-byte aligned.
+ *  - Every call that touches the GPU is asynchronous on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and never synchronises, except
+ *    kvc_last_device_error.  Inputs must stay alive until the stream passes them.
+ *  - The host-side slot map is updated when the call is made, so the call order
+ *    defines the cache state; a caller must not reorder the work across streams.
+ *  - Errors are returned as kvc_status values, never by aborting.  A call that
+ *    returns an error has changed nothing: neither the slot map nor (apart from
+ *    KVC_ECUDA after a launch) any device memory.
+ *  - One kvc_cache is used by one host thread at a time.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvc_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_EINVAL = -1,       /* bad sizes, null pointers, dtype mismatch, misalignment */
+  KVC_ESTATE = -2,       /* the call is not valid in the cache's current state */
+  KVC_ECUDA = -3,        /* a CUDA launch / runtime error */
+  KVC_ETIMEOUT = -4,     /* a kernel's bounded wait ran out (device error word set) */
+  KVC_EUNSUPPORTED = -5  /* valid request outside what the kernels implement */
+} kvc_status;
+
+typedef enum { KVC_BF16 = 0, KVC_FP4 = 1 } kvc_dtype;
+
+#define KVC_MAX_WINDOW 16 /* ring slots W <= 16 */
+#define KVC_WS_WORDS 1024 /* device workspace words (int32) per cache */
+#define KVC_QUANT_WS_WORDS 256 /* scratch words kvc_quant_fp4 needs */
+#define KVC_INIT_MAGIC 0x4B564331
+
+typedef struct kvc_cache {
+  /* ---- geometry: set by the caller before kvc_init ---- */
+  int32_t heads;            /* H >= 1 */
+  int32_t head_dim;         /* D, a multiple of 16; attention supports 64 and 128 */
+  int32_t tokens_per_frame; /* latent tokens of one frame (1560 = 30 x 52 for LongLive-1.3B) */
+  int32_t chunk_frames;     /* frames per chunk; the sink is exactly one chunk */
+  int32_t window_chunks;    /* W, 1..KVC_MAX_WINDOW ring slots, the current chunk included */
+  int32_t dtype;            /* kvc_dtype */
+  /* ---- device buffers: caller-allocated, sizes from kvc_cache_bytes ---- */
+  void* k;
+  void* v;
+  uint8_t* k_scale;  /* FP4 only, else NULL */
+  uint8_t* v_scale;  /* FP4 only, else NULL */
+  float* k_gscale;   /* FP4 only, [1 + W], else NULL */
+  float* v_gscale;   /* FP4 only, [1 + W], else NULL */
+  int32_t* dev_ws;   /* KVC_WS_WORDS int32, zero-filled by the caller before kvc_init;
+                        word 0 is the device error word, the rest is reduction scratch */
+  /* ---- options ---- */
+  int32_t scrub_on_evict; /* nonzero: kvc_evict overwrites the freed slot with NaN */
+  /* ---- library-maintained state: read-only for the caller ---- */
+  int32_t init_magic;
+  int64_t chunk_of_region[1 + KVC_MAX_WINDOW]; /* -1 = empty */
+} kvc_cache;
+
+/* sizeof(kvc_cache) as compiled into the library (lets bindings check the layout). */
+size_t kvc_sizeof_cache(void);
+
+/* Bytes of one device buffer of a cache with this geometry.
+ * which: 0 k, 1 v, 2 k_scale, 3 v_scale, 4 k_gscale, 5 v_gscale, 6 dev_ws.
+ * Returns 0 for a buffer the dtype does not use or for an invalid geometry. */
+size_t kvc_cache_bytes(const kvc_cache* c, int32_t which);
+
+/* Validate geometry and buffers, mark every region empty.  No GPU work.
+ * KVC_EINVAL on a bad geometry or a missing / misaligned buffer. */
+int32_t kvc_init(kvc_cache* c);
+
+/* Append chunk `chunk_idx`: k_chunk, v_chunk are device bf16 [Tc][H][D]
+ * (post-norm, post-RoPE keys, as the layer produced them).  The sink is chunk 0;
+ * chunk c >= 1 goes to ring slot (c-1) % W.  Allowed: chunk 0 into an empty
+ * cache; the newest chunk again (overwrite, one call per denoise step); the next
+ * chunk once its slot is empty (evict the oldest window chunk first).  Else
+ * KVC_ESTATE.  bf16 cache: a 128-bit vectorised copy.  FP4 cache: the chunk's K
+ * and V are quantised (tensor amax -> fp32 gscale[region], E4M3 block scales,
+ * E2M1 codes; the encode rule is kvc_quant_fp4's). */
+int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
+                   kvc_stream_t stream);
+
+/* Evict chunk `chunk_idx`, which must be the oldest window chunk (the sink is
+ * never evicted: KVC_ESTATE).  Moves no data: the slot is marked empty.  With
+ * scrub_on_evict set, the slot's rows are overwritten with NaN (bf16 0x7FC0;
+ * FP4: codes 0, scales 0x7F) so a stale read would show. */
+int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
+
+/* out = softmax(softmax_scale * q K^T) V per head, over the visible keys: the
+ * sink region plus every occupied window slot (no mask inside that set; keys are
+ * read in physical order, which softmax does not see).  q, out: device bf16
+ * [tq][H][D]; tq >= 0 (0 is a no-op).  FP4 caches are dequantised inside the tile
+ * load.  Attention supports D in {64, 128} (else KVC_EUNSUPPORTED); the sink
+ * must be present (else KVC_ESTATE).  A kernel wait that runs out leaves
+ * KVC_ETIMEOUT for kvc_last_device_error. */
+int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
+                     float softmax_scale, kvc_stream_t stream);
+
+/* KV recache at a prompt switch: for the n chunks listed in chunk_ids (host
+ * int64, logical order: sink first, then window chunks oldest -> newest; must be
+ * exactly the chunks in the cache, else KVC_ESTATE):
+ *   [K | V] = hidden @ w_kv;  K <- RoPE3D(RMSNorm(K) * gamma_k);  written to the
+ *   chunks' regions.
+ * hidden: device bf16 [n*Tc][H*D]; w_kv: device bf16 [H*D][2*H*D], the K columns
+ * first; gamma_k: device fp32 [H*D] or NULL (= ones).  RMSNorm spans the whole
+ * H*D-wide K row: x / sqrt(mean(x^2) + eps).  3D RoPE: token t of chunk c is at
+ * frame c*chunk_frames + t / tokens_per_frame, row (t % tpf) / grid_w, column
+ * t % grid_w (grid_h * grid_w == tokens_per_frame); the D/2 rotation pairs
+ * (adjacent elements) are split into [frame | row | column] bands of
+ * (P - 2*(P/3), P/3, P/3) pairs, P = D/2; in a band of b dims pair j turns by
+ * position * rope_theta^(-2j/b).  bf16 caches only (FP4: KVC_EUNSUPPORTED). */
+int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const float* gamma_k,
+                    float eps, const int64_t* chunk_ids, int32_t n, int32_t grid_h,
+                    int32_t grid_w, float rope_theta, kvc_stream_t stream);
+
+/* FP4-encode n bf16 values (device x, n % 16 == 0, n >= 16) as one tensor:
+ *   amax = max|x|;  g = fl32(amax / 2688);   (g == 0: all codes and scales 0)
+ *   per 16-block b: s = E4M3_rne_satfinite(fl32(fl32(amax_b / 6) / g));
+ *   s == 0 or fl32(s*g) == 0: codes 0;  else t = fl32(|x| * fl32(1 / fl32(s*g))),
+ *   code = signbit(x) << 3 | E2M1_rne_satfinite(t).
+ * codes: device uint8 [n/2] (element 2i in the low nibble); scales: device uint8
+ * [n/16]; gscale: device float [1]; ws: device scratch of KVC_QUANT_WS_WORDS
+ * int32 words that the call overwrites (per-CTA partial maxima; calls that share
+ * a ws must be stream-ordered).  n up to 2^31 * 16. */
+int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, float* gscale,
+                      int32_t* ws, kvc_stream_t stream);
+
+/* Synchronise `stream`, read and clear the cache's device error word.
+ * KVC_OK, KVC_ETIMEOUT (a kernel wait ran out), or KVC_ECUDA (a sticky CUDA error). */
+int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream);
+
+/* Diagnostic: one CTA waits on an mbarrier phase that nothing completes, with the
+ * same bounded wait the kernels use but a limit of `limit_us` microseconds
+ * (1..2000000), then records the timeout in dev_ws[0] and exits.  Exercises the
+ * watchdog path without hanging the GPU. */
+int32_t kvc_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, kvc_stream_t stream);
+
+/* Human-readable name of a kvc_status value. */
+const char* kvc_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

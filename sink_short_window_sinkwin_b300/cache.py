@@ -1,0 +1,136 @@
+"""Torch-facing wrapper of the C ABI: device buffers come from PyTorch, every
+step of the path runs in the library's kernels.  Methods only marshal pointers,
+sizes and the current CUDA stream, then raise ``KvcError`` on a bad status.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import KVC_BF16, KVC_FP4, KvcCache, check, lib
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _require(t: torch.Tensor, dtype, shape, name: str):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+class KVCache:
+    """One layer's sink + short-window cache (bf16 or FP4) on a CUDA device.
+
+    Region 0 holds the sink chunk; chunk c >= 1 lives in ring slot (c-1) % W.
+    """
+
+    def __init__(self, heads: int, head_dim: int, tokens_per_frame: int, chunk_frames: int,
+                 window_chunks: int, dtype: str = "bf16", device="cuda", scrub_on_evict=False):
+        self.c = KvcCache()
+        c = self.c
+        c.heads, c.head_dim = heads, head_dim
+        c.tokens_per_frame, c.chunk_frames = tokens_per_frame, chunk_frames
+        c.window_chunks = window_chunks
+        c.dtype = {"bf16": KVC_BF16, "fp4": KVC_FP4}[dtype]
+        c.scrub_on_evict = 1 if scrub_on_evict else 0
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.H, self.D = heads, head_dim
+        self.Tc = tokens_per_frame * chunk_frames
+        self.W = window_chunks
+        self.S = (1 + window_chunks) * self.Tc
+        L = lib()
+        nbytes = [L.kvc_cache_bytes(ctypes.byref(c), i) for i in range(7)]
+        if nbytes[0] == 0:
+            raise ValueError("invalid cache geometry")
+        if dtype == "bf16":
+            self.k = torch.zeros((self.S, heads, head_dim), dtype=torch.bfloat16, device=self.device)
+            self.v = torch.zeros_like(self.k)
+            self.k_scale = self.v_scale = self.k_gscale = self.v_gscale = None
+        else:
+            self.k = torch.zeros((self.S, heads, head_dim // 2), dtype=torch.uint8, device=self.device)
+            self.v = torch.zeros_like(self.k)
+            self.k_scale = torch.zeros((self.S, heads, head_dim // 16), dtype=torch.uint8,
+                                       device=self.device)
+            self.v_scale = torch.zeros_like(self.k_scale)
+            self.k_gscale = torch.zeros(1 + window_chunks, dtype=torch.float32, device=self.device)
+            self.v_gscale = torch.zeros_like(self.k_gscale)
+        self.ws = torch.zeros(_abi.KVC_WS_WORDS, dtype=torch.int32, device=self.device)
+        for name, t, nb in (("k", self.k, nbytes[0]), ("v", self.v, nbytes[1]),
+                            ("k_scale", self.k_scale, nbytes[2]), ("v_scale", self.v_scale, nbytes[3]),
+                            ("k_gscale", self.k_gscale, nbytes[4]), ("v_gscale", self.v_gscale, nbytes[5]),
+                            ("dev_ws", self.ws, nbytes[6])):
+            got = 0 if t is None else t.numel() * t.element_size()
+            if got != nb:
+                raise RuntimeError(f"{name}: {got} bytes allocated, library wants {nb}")
+            setattr(c, name, 0 if t is None else t.data_ptr())
+        check(L.kvc_init(ctypes.byref(c)), "kvc_init")
+
+    # -- state --------------------------------------------------------------
+    @property
+    def chunk_of_region(self) -> list[int]:
+        return [int(self.c.chunk_of_region[i]) for i in range(1 + self.W)]
+
+    # -- calls ---------------------------------------------------------------
+    def append(self, k: torch.Tensor, v: torch.Tensor, chunk_idx: int, stream=None) -> None:
+        shp = (self.Tc, self.H, self.D)
+        _require(k, torch.bfloat16, shp, "k")
+        _require(v, torch.bfloat16, shp, "v")
+        check(lib().kvc_append(ctypes.byref(self.c), _ptr(k), _ptr(v), int(chunk_idx), _stream(stream)),
+              "kvc_append")
+
+    def evict(self, chunk_idx: int, stream=None) -> None:
+        check(lib().kvc_evict(ctypes.byref(self.c), int(chunk_idx), _stream(stream)), "kvc_evict")
+
+    def attn(self, q: torch.Tensor, softmax_scale: float, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+        tq = q.shape[0]
+        _require(q, torch.bfloat16, (tq, self.H, self.D), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        _require(out, torch.bfloat16, (tq, self.H, self.D), "out")
+        check(lib().sinkwin_attn(ctypes.byref(self.c), _ptr(q), _ptr(out), int(tq),
+                                 float(softmax_scale), _stream(stream)), "sinkwin_attn")
+        return out
+
+    def recache(self, hidden: torch.Tensor, w_kv: torch.Tensor, gamma: torch.Tensor | None,
+                chunk_ids, grid_h: int, grid_w: int, eps: float = 1e-6, theta: float = 10000.0,
+                stream=None) -> None:
+        n = len(chunk_ids)
+        HD = self.H * self.D
+        _require(hidden, torch.bfloat16, (n * self.Tc, HD), "hidden")
+        _require(w_kv, torch.bfloat16, (HD, 2 * HD), "w_kv")
+        if gamma is not None:
+            _require(gamma, torch.float32, (HD,), "gamma")
+        ids = (ctypes.c_int64 * n)(*[int(x) for x in chunk_ids])
+        check(lib().kvc_recache(ctypes.byref(self.c), _ptr(hidden), _ptr(w_kv), _ptr(gamma),
+                                float(eps), ids, n, int(grid_h), int(grid_w), float(theta),
+                                _stream(stream)), "kvc_recache")
+
+    def last_device_error(self, stream=None) -> int:
+        return int(lib().kvc_last_device_error(ctypes.byref(self.c), _stream(stream)))
+
+
+def quant_fp4(x: torch.Tensor, stream=None):
+    """FP4-encode a bf16 tensor (numel % 16 == 0): returns (codes u8 [n/2],
+    scales u8 [n/16], gscale f32 [1])."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA bf16 tensor")
+    n = x.numel()
+    codes = torch.empty(n // 2, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(n // 16, dtype=torch.uint8, device=x.device)
+    g = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = torch.empty(_abi.KVC_QUANT_WS_WORDS, dtype=torch.int32, device=x.device)
+    check(lib().kvc_quant_fp4(_ptr(x), int(n), _ptr(codes), _ptr(scales), _ptr(g), _ptr(ws),
+                              _stream(stream)), "kvc_quant_fp4")
+    return codes, scales, g

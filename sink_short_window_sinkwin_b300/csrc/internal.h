@@ -1,0 +1,90 @@
+// Launchers shared between the C-ABI layer (kvc_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvc.h"
+
+namespace kvc {
+
+constexpr int kMaxSeg = 1 + KVC_MAX_WINDOW;
+
+// A run of visible cache rows [row0, row0 + rows).
+struct Seg {
+  int32_t row0;
+  int32_t rows;
+};
+
+// ---- bandwidth kernels (kernels_mem.cu) ----
+// dst[i] = src[i] for two tensors of `bytes` bytes each (16-byte aligned, bytes % 16 == 0)
+cudaError_t launch_copy2(void* dst0, const void* src0, void* dst1, const void* src1, size_t bytes,
+                         cudaStream_t st);
+// fill two byte ranges with a repeated 16-bit pattern / byte pattern
+cudaError_t launch_fill2_u16(void* d0, void* d1, size_t bytes, uint16_t pattern, cudaStream_t st);
+cudaError_t launch_fill2_u8(void* d0, void* d1, size_t bytes, uint8_t pattern, cudaStream_t st);
+
+// FP4 encode of up to two tensors (x1 may be null), n elements each, n % 16 == 0.
+// ws: 2 * kQuantPartials int32 words (per-CTA partial maxima).
+constexpr int kQuantPartials = 256;
+struct QuantJob {
+  const void* x;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* gscale;
+};
+cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
+                             cudaStream_t st);
+
+// ---- attention (kernels_attn.cu) ----
+struct AttnLaunch {
+  const void* q;        // bf16 [tq][H][D]
+  void* out;            // bf16 [tq][H][D]
+  int32_t tq, H, D;
+  int32_t S;            // physical cache rows
+  float scale_log2;     // softmax_scale * log2(e)
+  int32_t nseg;
+  Seg seg[kMaxSeg];
+  int32_t* dev_err;
+  // bf16 cache
+  const void* k;
+  const void* v;
+  // FP4 cache
+  int32_t fp4;
+  const uint8_t* k_scale;
+  const uint8_t* v_scale;
+  const float* k_gscale;
+  const float* v_gscale;
+  int32_t chunk_tokens;  // rows per region (FP4: region of a row -> its tensor scale)
+};
+cudaError_t launch_sinkwin_attn(const AttnLaunch& a, cudaStream_t st);
+
+// ---- recache (kernels_recache.cu) ----
+struct RecacheLaunch {
+  const void* hidden;  // bf16 [n*Tc][H*D]
+  const void* w_kv;    // bf16 [H*D][2*H*D]
+  const float* gamma;  // fp32 [H*D] or null
+  float eps, theta;
+  int32_t rows, H, D, Tc, tpf, chunk_frames, grid_w;
+  int32_t n;
+  int64_t chunk_id[kMaxSeg];
+  int32_t region[kMaxSeg];
+  void* k;  // bf16 cache [S][H][D]
+  void* v;
+  int32_t* dev_err;
+};
+cudaError_t launch_recache(const RecacheLaunch& r, cudaStream_t st);
+
+// ---- diagnostics ----
+cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st);
+
+// driver entry point for tensor-map encoding (resolved once through the runtime)
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                         uint32_t box1, uint32_t box2, bool swizzle128);
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                         uint64_t stride1_bytes, uint32_t box0, uint32_t box1, bool swizzle128);
+
+}  // namespace kvc

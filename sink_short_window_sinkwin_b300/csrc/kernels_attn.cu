@@ -1,0 +1,560 @@
+// Sink + short-window chunk attention on tcgen05 tensor cores.
+//
+// LongLive summary page (yunpan.plus), 方法 §3 高效长推理: each new chunk's
+// queries attend to the frame-sink tokens (first chunk, kept for good) joined
+// with a short window of recent chunks; the cost is bounded by the window.
+// Here: O = softmax(tau Q K^T) V per head over the visible cache rows, exact up
+// to floating-point rounding (bf16 operands, fp32 accumulation and softmax).
+//
+// One CTA = one head x two 128-row query tiles ("slots") that share every K/V
+// tile.  Warp roles (320 threads):
+//   warps 0-3  softmax of slot 0 (thread i owns query row i: TMEM lane i)
+//   warps 4-7  softmax of slot 1
+//   warp  8    TMA producer: Q once, then K/V tiles of 128 keys, 2-stage ring
+//   warp  9    TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 10-13 (FP4 cache only) dequantise K/V tiles into the smem ring
+// TMEM (512 columns): S0 [0,128) O0 [128,256) S1 [256,384) O1 [384,512);
+// P (bf16) overwrites the first 64 columns of S and feeds the P*V MMA from TMEM.
+// The running max is only moved when it grows by more than 2^8 (log2 domain),
+// so O is rescaled in TMEM rarely.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int BM = 128;        // query rows per slot
+constexpr int BN = 128;        // keys per K/V tile
+constexpr int kStages = 2;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDequantWarp0 = 10;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct AttnParams {
+  int32_t tq, H, D, S, nt;  // nt: K/V tiles over all segments
+  int32_t nseg;
+  Seg seg[kMaxSeg];
+  float scale_log2;
+  __nv_bfloat16* out;
+  int32_t* dev_err;
+  // FP4 cache
+  const uint8_t* kc;
+  const uint8_t* vc;
+  const uint8_t* ks;
+  const uint8_t* vs;
+  const float* kg;
+  const float* vg;
+  int32_t Tc;
+};
+
+template <int D>
+struct __align__(1024) AttnSmem {
+  static constexpr int DB = D / 64;  // 128-byte swizzle blocks along the head dim
+  __nv_bfloat16 q[2][DB][BM * 64];
+  __nv_bfloat16 k[kStages][DB][BN * 64];
+  __nv_bfloat16 v[kStages][DB][BN * 64];
+  uint64_t bar_q;
+  uint64_t bar_kfull[kStages], bar_kempty[kStages];
+  uint64_t bar_vfull[kStages], bar_vempty[kStages];
+  uint64_t bar_s[2], bar_p[2];
+  uint64_t bar_drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+// Walk the visible segments tile by tile.
+struct KvCursor {
+  int seg = 0, off = 0;
+  __device__ __forceinline__ int row0(const AttnParams& p) const { return p.seg[seg].row0 + off; }
+  __device__ __forceinline__ int valid(const AttnParams& p) const {
+    return min(BN, p.seg[seg].rows - off);
+  }
+  __device__ __forceinline__ void next(const AttnParams& p) {
+    off += BN;
+    if (off >= p.seg[seg].rows) {
+      ++seg;
+      off = 0;
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// FP4 tile dequantisation: thread i writes key row i of a K or V tile as bf16
+// in the 128-byte-swizzled layout the MMA descriptors expect.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(d)
+      : "r"(byte));
+  return d;
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+  if (e == 0) return (float)m * 0.001953125f;
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+template <int D>
+__device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r, int grow,
+                                            bool live, const uint8_t* codes, const uint8_t* scales,
+                                            const float* gsc, const AttnParams& p, int h) {
+  constexpr int DB = D / 64;
+  uint8_t* base = reinterpret_cast<uint8_t*>(dst);
+  if (!live) {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const int db = c >> 3, ch = c & 7;
+      *reinterpret_cast<uint4*>(base + db * (BN * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const float g = gsc[grow / p.Tc];
+  const uint8_t* crow = codes + ((size_t)grow * p.H + h) * (D / 2);
+  const uint8_t* srow = scales + ((size_t)grow * p.H + h) * (D / 16);
+  uint32_t sc[D / 16];
+  if constexpr (D == 128) {
+    const uint2 s8 = *reinterpret_cast<const uint2*>(srow);
+    const uint32_t sw[2] = {s8.x, s8.y};
+#pragma unroll
+    for (int b = 0; b < 8; ++b) sc[b] = (sw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+  } else {
+    const uint32_t s4 = *reinterpret_cast<const uint32_t*>(srow);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) sc[b] = (s4 >> (8 * b)) & 0xFFu;
+  }
+#pragma unroll
+  for (int q16 = 0; q16 < D / 32; ++q16) {  // 16 code bytes = 32 elements = 2 blocks
+    const uint4 cw = *reinterpret_cast<const uint4*>(crow + q16 * 16);
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // one 16-element block -> two 16-byte chunks
+      const float f = e4m3_to_f32(sc[q16 * 2 + half]) * g;
+      uint32_t outw[8];
+#pragma unroll
+      for (int bi = 0; bi < 8; ++bi) {
+        const uint32_t word = w[half * 2 + (bi >> 2)];
+        const uint32_t h2 = e2m1x2_to_f16x2((word >> (8 * (bi & 3))) & 0xFFu);
+        const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+        const float2 fv = __half22float2(hv);
+        outw[bi] = pack_bf16x2(fv.x * f, fv.y * f);
+      }
+      const int e0 = q16 * 32 + half * 16;  // first element of this block
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int c = (e0 >> 3) + part;  // 16-byte chunk index along D
+        const int db = c >> 3, ch = c & 7;
+        *reinterpret_cast<uint4*>(base + db * (BN * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+            make_uint4(outw[part * 4 + 0], outw[part * 4 + 1], outw[part * 4 + 2],
+                       outw[part * 4 + 3]);
+      }
+    }
+  }
+}
+
+template <int D, bool kFp4>
+__global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
+    sinkwin_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
+  using Smem = AttnSmem<D>;
+  constexpr int DB = Smem::DB;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.x * (2 * BM);
+  const bool active1 = (m0 + BM) < p.tq;
+  const int nt = p.nt;
+  const uint32_t kvfull_count = kFp4 ? 128u : 1u;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.bar_kfull[s], kvfull_count);
+      mbar_init(&sm.bar_vfull[s], kvfull_count);
+      mbar_init(&sm.bar_kempty[s], 1);
+      mbar_init(&sm.bar_vempty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.bar_s[s], 1);
+      mbar_init(&sm.bar_p[s], BM);
+    }
+    mbar_init(&sm.bar_drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    if (!kFp4) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Watchdog wd{&sm.abort_flag, p.dev_err};
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t qbytes = (active1 ? 2u : 1u) * DB * BM * 64 * 2;
+      mbar_expect_tx(&sm.bar_q, qbytes);
+      for (int s = 0; s < (active1 ? 2 : 1); ++s)
+        for (int db = 0; db < DB; ++db)
+          tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
+      int issued = 0;
+      if (!kFp4) {
+        KvCursor cur;
+        const uint32_t tbytes = DB * BN * 64 * 2;
+        for (int t = 0; t < nt; ++t) {
+          const int st = t & 1, n = t >> 1;
+          if (t >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) break;
+          mbar_expect_tx(&sm.bar_kfull[st], tbytes);
+          for (int db = 0; db < DB; ++db)
+            tma_load_3d(&sm.k[st][db][0], &tmK, &sm.bar_kfull[st], db * 64, h, cur.row0(p));
+          if (t >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
+            issued = -(t + 1);  // K of tile t issued, V not
+            break;
+          }
+          mbar_expect_tx(&sm.bar_vfull[st], tbytes);
+          for (int db = 0; db < DB; ++db)
+            tma_load_3d(&sm.v[st][db][0], &tmV, &sm.bar_vfull[st], db * 64, h, cur.row0(p));
+          cur.next(p);
+          issued = t + 1;
+        }
+        // teardown: every copy this thread started must land before the CTA exits
+        if (sm.abort_flag) {
+          const int nk = issued >= 0 ? issued : -issued;
+          const int nv = issued >= 0 ? issued : (-issued - 1);
+          for (int st = 0; st < kStages; ++st) {
+            const int ck = nk > st ? (nk - st + 1) / 2 : 0;  // uses of stage st
+            const int cv = nv > st ? (nv - st + 1) / 2 : 0;
+            if (ck) mbar_drain(&sm.bar_kfull[st], (ck - 1) & 1);
+            if (cv) mbar_drain(&sm.bar_vfull[st], (cv - 1) & 1);
+          }
+        }
+      }
+      mbar_drain(&sm.bar_q, 0);
+    }
+  } else if (kFp4 && warp >= kDequantWarp0) {
+    // ------------------------------------------------------------ FP4 dequant producer
+    const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
+    KvCursor cur;
+    for (int t = 0; t < nt; ++t) {
+      const int st = t & 1, n = t >> 1;
+      const int grow = cur.row0(p) + r;
+      const bool live = r < cur.valid(p);
+      if (t >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) break;
+      dequant_row<D>(sm.k[st], r, grow, live, p.kc, p.ks, p.kg, p, h);
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.bar_kfull[st]);
+      if (t >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) break;
+      dequant_row<D>(sm.v[st], r, grow, live, p.vc, p.vs, p.vg, p, h);
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.bar_vfull[st]);
+      cur.next(p);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+      const uint32_t tS[2] = {tmem, tmem + 256};
+      const uint32_t tO[2] = {tmem + 128, tmem + 384};
+      auto qk = [&](int slot, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(smem_u32(&sm.q[slot][kk >> 2][0]) + koff, 0, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(&sm.k[st][kk >> 2][0]) + koff, 0, 1024);
+          mma_bf16_ss(tS[slot], ad, bd, idesc_qk, kk > 0);
+        }
+      };
+      auto pv = [&](int slot, int st, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_sw128(smem_u32(&sm.v[st][0][0]) + kk * 2048, BN * 64 * 2, 1024);
+          mma_bf16_ts(tO[slot], tS[slot] + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0, wd) && mbar_wait(&sm.bar_kfull[0], 0, wd);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        mma_commit(&sm.bar_s[0]);
+        if (active1) {
+          qk(1, 0);
+          mma_commit(&sm.bar_s[1]);
+        }
+        mma_commit(&sm.bar_kempty[0]);
+        for (int t = 0; t < nt && ok; ++t) {
+          const int st = t & 1, ph = (t >> 1) & 1;
+          const int nst = (t + 1) & 1, nph = ((t + 1) >> 1) & 1;
+          const bool more = t + 1 < nt;
+          ok = mbar_wait(&sm.bar_p[0], t & 1, wd) && mbar_wait(&sm.bar_vfull[st], ph, wd);
+          if (!ok) break;
+          tc_fence_after();
+          pv(0, st, t > 0);
+          if (more) {
+            ok = mbar_wait(&sm.bar_kfull[nst], nph, wd);
+            if (!ok) break;
+            tc_fence_after();
+            qk(0, nst);
+          }
+          mma_commit(&sm.bar_s[0]);
+          if (active1) {
+            ok = mbar_wait(&sm.bar_p[1], t & 1, wd);
+            if (!ok) break;
+            tc_fence_after();
+            pv(1, st, t > 0);
+            mma_commit(&sm.bar_vempty[st]);
+            if (more) qk(1, nst);
+            mma_commit(&sm.bar_s[1]);
+          } else {
+            mma_commit(&sm.bar_vempty[st]);
+          }
+          if (more) mma_commit(&sm.bar_kempty[nst]);
+        }
+      }
+      // drain: every MMA issued above completes before TMEM is released
+      mma_commit(&sm.bar_drain);
+      mbar_drain(&sm.bar_drain, 0);
+    }
+  } else if (warp < kSoftmaxWarps) {
+    // ------------------------------------------------------------ softmax
+    const int slot = warp >> 2;
+    const int wq = warp & 3;
+    const int row = threadIdx.x & (BM - 1);
+    if (slot == 0 || active1) {
+      const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+      const uint32_t tS = tmem + slot * 256 + lane_off;
+      const uint32_t tO = tS + 128;
+      const float c = p.scale_log2;
+      float m_ref = -INFINITY, l = 0.0f;
+      bool ok = true;
+      // keep a stale running max unless it grew by more than 2^8; then rescale
+      // O in TMEM (warp-collective ld/st, lanes that do not move keep factor 1)
+      auto rescale_if_needed = [&](int t, float mx_scaled, float& m_ref, float& l, uint32_t tO) {
+        const float m_new = fmaxf(m_ref, mx_scaled);
+        if (t == 0) {
+          m_ref = m_new;
+          return;
+        }
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;
+          if (need) m_ref = m_new;
+          l *= alpha;
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t o[32];
+            tmem_ld32(tO + j * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + j * 32, o);
+          }
+          tmem_st_wait();
+        }
+      };
+      KvCursor cur;
+      for (int t = 0; t < nt; ++t) {
+        if (!mbar_wait(&sm.bar_s[slot], t & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int valid = cur.valid(p);
+        if (!kFp4 && slot == 0 && valid < BN) {
+          // key rows past the segment end may hold anything (NaN scrub,
+          // never-written memory): zero them in the V stage before P*V
+          const int st = t & 1;
+          if (!mbar_wait(&sm.bar_vfull[st], (t >> 1) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vb = reinterpret_cast<uint8_t*>(&sm.v[st][0][0]);
+          for (int idx = row; idx < (BN - valid) * 8 * DB; idx += BM) {
+            const int rr = valid + idx / (8 * DB);
+            const int rem = idx % (8 * DB);
+            *reinterpret_cast<uint4*>(vb + (rem >> 3) * (BN * 128) + rr * 128 + ((rem & 7) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        if constexpr (!kFp4) {
+          // one pass: the whole S row lives in registers
+          uint32_t sr[BN];
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j)
+            tmem_ld32(tS + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[j * 32]));
+          tmem_ld_wait();
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < BN; ++j) {
+            if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(sr[j]));
+          }
+          rescale_if_needed(t, mx * c, m_ref, l, tO);
+          const float neg = -m_ref;
+          float sum = 0.0f;
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j * 64 + 2 * e]), c, neg));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j * 64 + 2 * e + 1]), c, neg));
+              sum += p0 + p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS + j * 32, pk);
+          }
+          l += sum;
+        } else {
+          // two passes over 32-column chunks (fewer live registers)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) {
+            uint32_t sr[32];
+            tmem_ld32(tS + j * 32, sr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (j * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(sr[e]));
+          }
+          rescale_if_needed(t, mx * c, m_ref, l, tO);
+          const float neg = -m_ref;
+          float sum = 0.0f;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) {
+            // chunk j (keys 32j..32j+31) -> P columns 16j..16j+15, which only
+            // overlap S columns already consumed
+            uint32_t sr[32];
+            tmem_ld32(tS + j * 32, sr);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int k0 = j * 32 + 2 * e;
+              const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e]), c, neg)) : 0.0f;
+              const float p1 =
+                  k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), c, neg)) : 0.0f;
+              sum += p0 + p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + j * 16, pk);
+          }
+          l += sum;
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.bar_p[slot]);
+        cur.next(p);
+      }
+      if (ok && mbar_wait(&sm.bar_s[slot], nt & 1, wd)) {
+        tc_fence_after();
+        const int grow = m0 + slot * BM + row;
+        const float inv_l = 1.0f / l;
+        __nv_bfloat16* dst = p.out + ((size_t)grow * p.H + h) * D;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tO + j * 32, o);
+          tmem_ld_wait();
+          if (grow < p.tq) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(dst + j * 32 + e) = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool kFp4>
+cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
+  CUtensorMap tq{}, tk{}, tv{};
+  const uint64_t rs = (uint64_t)a.H * a.D * 2;  // bytes per token row
+  if (!encode_tmap_3d_bf16(&tq, a.q, a.D, a.H, a.tq, (uint64_t)a.D * 2, rs, 64, 1, BM, true))
+    return cudaErrorInvalidValue;
+  if (!kFp4) {
+    if (!encode_tmap_3d_bf16(&tk, a.k, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_3d_bf16(&tv, a.v, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
+      return cudaErrorInvalidValue;
+  } else {
+    tk = tq;  // unused
+    tv = tq;
+  }
+  AttnParams p{};
+  p.tq = a.tq;
+  p.H = a.H;
+  p.D = a.D;
+  p.S = a.S;
+  p.nseg = a.nseg;
+  int nt = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    p.seg[i] = a.seg[i];
+    nt += (a.seg[i].rows + BN - 1) / BN;
+  }
+  p.nt = nt;
+  p.scale_log2 = a.scale_log2;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.dev_err = a.dev_err;
+  p.kc = static_cast<const uint8_t*>(a.k);
+  p.vc = static_cast<const uint8_t*>(a.v);
+  p.ks = a.k_scale;
+  p.vs = a.v_scale;
+  p.kg = a.k_gscale;
+  p.vg = a.v_gscale;
+  p.Tc = a.chunk_tokens;
+  const size_t smem = sizeof(AttnSmem<D>) + 1024;
+  auto kern = sinkwin_attn_kernel<D, kFp4>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.tq + 2 * BM - 1) / (2 * BM), a.H);
+  kern<<<grid, kFp4 ? 448 : 320, smem, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sinkwin_attn(const AttnLaunch& a, cudaStream_t st) {
+  if (a.D == 128) return a.fp4 ? launch_attn_t<128, true>(a, st) : launch_attn_t<128, false>(a, st);
+  if (a.D == 64) return a.fp4 ? launch_attn_t<64, true>(a, st) : launch_attn_t<64, false>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

@@ -1,0 +1,404 @@
+// C ABI: argument validation, the host-side slot map of the sink + window ring,
+// and the kernel launches.  Every entry point validates first, launches second,
+// and only then commits the new slot-map state, so an error changes nothing.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "kvc.h"
+#include "ptx.cuh"
+
+namespace kvc {
+
+// ---------------------------------------------------------------------------
+// tensor maps (cuTensorMapEncodeTiled, resolved through the runtime so the
+// library does not link the driver library directly)
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                         uint32_t box1, uint32_t box2, bool swizzle128) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                         uint64_t stride1_bytes, uint32_t box0, uint32_t box1, bool swizzle128) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {d0, d1};
+  cuuint64_t strides[1] = {stride1_bytes};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// watchdog self-test: one CTA waits for a phase nothing completes
+// ---------------------------------------------------------------------------
+__global__ void watchdog_selftest_kernel(int32_t* dev_ws, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Watchdog wd{&abort_flag, dev_ws};
+    mbar_wait(&bar, 0, wd, limit_ns);  // no arrive ever happens: runs out
+  }
+}
+
+cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st) {
+  watchdog_selftest_kernel<<<1, 32, 0, st>>>(dev_ws, (uint64_t)limit_us * 1000ull);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+namespace {
+
+constexpr int32_t kMaxRows = 1 << 30;
+
+int64_t chunk_tokens(const kvc_cache* c) { return (int64_t)c->tokens_per_frame * c->chunk_frames; }
+int64_t cache_rows(const kvc_cache* c) { return (1 + (int64_t)c->window_chunks) * chunk_tokens(c); }
+
+bool geometry_ok(const kvc_cache* c) {
+  if (!c) return false;
+  if (c->heads < 1 || c->head_dim < 16 || c->head_dim % 16 != 0 || c->head_dim > 256) return false;
+  if (c->tokens_per_frame < 1 || c->chunk_frames < 1) return false;
+  if (c->window_chunks < 1 || c->window_chunks > KVC_MAX_WINDOW) return false;
+  if (c->dtype != KVC_BF16 && c->dtype != KVC_FP4) return false;
+  const int64_t S = cache_rows(c);
+  if (S <= 0 || S > kMaxRows) return false;
+  if (S * c->heads * (int64_t)c->head_dim > (int64_t(1) << 40)) return false;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ready(const kvc_cache* c) { return c && c->init_magic == KVC_INIT_MAGIC && geometry_ok(c); }
+
+int32_t region_of(int64_t chunk, int32_t W) { return chunk == 0 ? 0 : 1 + (int32_t)((chunk - 1) % W); }
+
+int64_t newest_chunk(const kvc_cache* c) {
+  int64_t m = -1;
+  for (int r = 0; r <= c->window_chunks; ++r) m = c->chunk_of_region[r] > m ? c->chunk_of_region[r] : m;
+  return m;
+}
+
+int64_t oldest_window_chunk(const kvc_cache* c) {
+  int64_t m = -1;
+  for (int r = 1; r <= c->window_chunks; ++r) {
+    const int64_t x = c->chunk_of_region[r];
+    if (x >= 0 && (m < 0 || x < m)) m = x;
+  }
+  return m;
+}
+
+// present chunks in logical order: sink first, then window chunks ascending
+int present_chunks(const kvc_cache* c, int64_t* out) {
+  int n = 0;
+  if (c->chunk_of_region[0] == 0) out[n++] = 0;
+  int64_t last = 0;
+  while (true) {
+    int64_t best = -1;
+    for (int r = 1; r <= c->window_chunks; ++r) {
+      const int64_t x = c->chunk_of_region[r];
+      if (x > last && (best < 0 || x < best)) best = x;
+    }
+    if (best < 0) break;
+    out[n++] = best;
+    last = best;
+  }
+  return n;
+}
+
+int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ECUDA; }
+
+size_t row_bytes(const kvc_cache* c, int which) {
+  const size_t hd = (size_t)c->heads * c->head_dim;
+  switch (which) {
+    case 0:
+    case 1:
+      return c->dtype == KVC_BF16 ? hd * 2 : hd / 2;
+    case 2:
+    case 3:
+      return c->dtype == KVC_FP4 ? hd / 16 : 0;
+    default:
+      return 0;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvc_sizeof_cache(void) { return sizeof(kvc_cache); }
+
+size_t kvc_cache_bytes(const kvc_cache* c, int32_t which) {
+  if (!geometry_ok(c)) return 0;
+  const size_t S = (size_t)cache_rows(c);
+  switch (which) {
+    case 0:
+    case 1:
+    case 2:
+    case 3:
+      return S * row_bytes(c, which);
+    case 4:
+    case 5:
+      return c->dtype == KVC_FP4 ? (size_t)(1 + c->window_chunks) * sizeof(float) : 0;
+    case 6:
+      return (size_t)KVC_WS_WORDS * sizeof(int32_t);
+    default:
+      return 0;
+  }
+}
+
+int32_t kvc_init(kvc_cache* c) {
+  if (!geometry_ok(c)) return KVC_EINVAL;
+  if (!c->k || !c->v || !c->dev_ws || !aligned16(c->k) || !aligned16(c->v) || !aligned16(c->dev_ws))
+    return KVC_EINVAL;
+  if (c->dtype == KVC_FP4) {
+    if (!c->k_scale || !c->v_scale || !c->k_gscale || !c->v_gscale) return KVC_EINVAL;
+    if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVC_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(c->k_gscale) & 3u) || (reinterpret_cast<uintptr_t>(c->v_gscale) & 3u))
+      return KVC_EINVAL;
+  }
+  for (int r = 0; r < 1 + KVC_MAX_WINDOW; ++r) c->chunk_of_region[r] = -1;
+  c->init_magic = KVC_INIT_MAGIC;
+  return KVC_OK;
+}
+
+int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
+                   kvc_stream_t stream) {
+  if (!ready(c) || !k_chunk || !v_chunk || !aligned16(k_chunk) || !aligned16(v_chunk) || chunk_idx < 0)
+    return KVC_EINVAL;
+  // state
+  if (c->chunk_of_region[0] != 0) {
+    if (chunk_idx != 0) return KVC_ESTATE;
+  } else {
+    const int64_t nw = newest_chunk(c);
+    if (chunk_idx != nw && chunk_idx != nw + 1) return KVC_ESTATE;
+  }
+  const int32_t r = region_of(chunk_idx, c->window_chunks);
+  const int64_t occ = c->chunk_of_region[r];
+  if (occ != -1 && occ != chunk_idx) return KVC_ESTATE;
+  // launch
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t Tc = chunk_tokens(c);
+  const int64_t n = Tc * c->heads * (int64_t)c->head_dim;  // elements per tensor
+  cudaError_t e;
+  if (c->dtype == KVC_BF16) {
+    const size_t off = (size_t)r * Tc * row_bytes(c, 0);
+    e = launch_copy2(static_cast<uint8_t*>(c->k) + off, k_chunk, static_cast<uint8_t*>(c->v) + off,
+                     v_chunk, (size_t)n * 2, st);
+  } else {
+    const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
+    const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
+    QuantJob jobs[2] = {
+        {k_chunk, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
+        {v_chunk, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
+    e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
+  }
+  if (e != cudaSuccess) return KVC_ECUDA;
+  c->chunk_of_region[r] = chunk_idx;
+  return KVC_OK;
+}
+
+int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream) {
+  if (!ready(c) || chunk_idx < 0) return KVC_EINVAL;
+  if (chunk_idx == 0) return KVC_ESTATE;
+  if (oldest_window_chunk(c) != chunk_idx) return KVC_ESTATE;
+  const int32_t r = region_of(chunk_idx, c->window_chunks);
+  if (c->chunk_of_region[r] != chunk_idx) return KVC_ESTATE;
+  if (c->scrub_on_evict) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t Tc = chunk_tokens(c);
+    cudaError_t e;
+    if (c->dtype == KVC_BF16) {
+      const size_t off = (size_t)r * Tc * row_bytes(c, 0);
+      e = launch_fill2_u16(static_cast<uint8_t*>(c->k) + off, static_cast<uint8_t*>(c->v) + off,
+                           (size_t)Tc * row_bytes(c, 0), 0x7FC0u, st);
+    } else {
+      const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
+      const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
+      e = launch_fill2_u8(static_cast<uint8_t*>(c->k) + coff, static_cast<uint8_t*>(c->v) + coff,
+                          (size_t)Tc * row_bytes(c, 0), 0x00u, st);
+      if (e == cudaSuccess)
+        e = launch_fill2_u8(c->k_scale + soff, c->v_scale + soff, (size_t)Tc * row_bytes(c, 2), 0x7Fu,
+                            st);
+    }
+    if (e != cudaSuccess) return KVC_ECUDA;
+  }
+  c->chunk_of_region[r] = -1;
+  return KVC_OK;
+}
+
+int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, float softmax_scale,
+                     kvc_stream_t stream) {
+  if (!ready(c) || tq < 0) return KVC_EINVAL;
+  if (tq == 0) return KVC_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out) || !std::isfinite(softmax_scale))
+    return KVC_EINVAL;
+  if (c->head_dim != 64 && c->head_dim != 128) return KVC_EUNSUPPORTED;
+  if (c->chunk_of_region[0] != 0) return KVC_ESTATE;
+  AttnLaunch a{};
+  a.q = q;
+  a.out = out;
+  a.tq = tq;
+  a.H = c->heads;
+  a.D = c->head_dim;
+  a.S = (int32_t)cache_rows(c);
+  a.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+  const int32_t Tc = (int32_t)chunk_tokens(c);
+  a.nseg = 0;
+  for (int r = 0; r <= c->window_chunks; ++r) {
+    if (c->chunk_of_region[r] < 0) continue;
+    const int32_t row0 = r * Tc;
+    if (a.nseg > 0 && a.seg[a.nseg - 1].row0 + a.seg[a.nseg - 1].rows == row0)
+      a.seg[a.nseg - 1].rows += Tc;
+    else
+      a.seg[a.nseg++] = Seg{row0, Tc};
+  }
+  a.dev_err = c->dev_ws;
+  a.k = c->k;
+  a.v = c->v;
+  a.fp4 = c->dtype == KVC_FP4;
+  a.k_scale = c->k_scale;
+  a.v_scale = c->v_scale;
+  a.k_gscale = c->k_gscale;
+  a.v_gscale = c->v_gscale;
+  a.chunk_tokens = Tc;
+  return cuda_status(launch_sinkwin_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const float* gamma_k,
+                    float eps, const int64_t* chunk_ids, int32_t n, int32_t grid_h, int32_t grid_w,
+                    float rope_theta, kvc_stream_t stream) {
+  if (!ready(c) || !hidden || !w_kv || !chunk_ids || n < 1 || n > 1 + c->window_chunks)
+    return KVC_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_kv) || (gamma_k && (reinterpret_cast<uintptr_t>(gamma_k) & 3u)))
+    return KVC_EINVAL;
+  if (grid_h < 1 || grid_w < 1 || (int64_t)grid_h * grid_w != c->tokens_per_frame) return KVC_EINVAL;
+  if (!(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta > 0.0f) || !std::isfinite(rope_theta))
+    return KVC_EINVAL;
+  if (c->dtype != KVC_BF16) return KVC_EUNSUPPORTED;
+  const int HD = c->heads * c->head_dim;
+  if (!((HD % 256 == 0 && HD / 256 <= 8) || (HD % 128 == 0 && HD / 128 <= 8) ||
+        (HD % 64 == 0 && HD / 64 <= 8)))
+    return KVC_EUNSUPPORTED;
+  if (c->head_dim / 2 > 128) return KVC_EUNSUPPORTED;
+  int64_t present[1 + KVC_MAX_WINDOW];
+  const int np = present_chunks(c, present);
+  if (np != n) return KVC_ESTATE;
+  for (int i = 0; i < n; ++i)
+    if (chunk_ids[i] != present[i]) return KVC_ESTATE;
+  RecacheLaunch rl{};
+  rl.hidden = hidden;
+  rl.w_kv = w_kv;
+  rl.gamma = gamma_k;
+  rl.eps = eps;
+  rl.theta = rope_theta;
+  rl.Tc = (int32_t)chunk_tokens(c);
+  rl.rows = n * rl.Tc;
+  rl.H = c->heads;
+  rl.D = c->head_dim;
+  rl.tpf = c->tokens_per_frame;
+  rl.chunk_frames = c->chunk_frames;
+  rl.grid_w = grid_w;
+  rl.n = n;
+  for (int i = 0; i < n; ++i) {
+    rl.chunk_id[i] = chunk_ids[i];
+    rl.region[i] = region_of(chunk_ids[i], c->window_chunks);
+  }
+  rl.k = c->k;
+  rl.v = c->v;
+  rl.dev_err = c->dev_ws;
+  return cuda_status(launch_recache(rl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, float* gscale,
+                      int32_t* ws, kvc_stream_t stream) {
+  if (!x || !codes || !scales || !gscale || !ws) return KVC_EINVAL;
+  if (n < 16 || n % 16 != 0 || n / 16 > (int64_t(1) << 31)) return KVC_EINVAL;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u) ||
+      (reinterpret_cast<uintptr_t>(gscale) & 3u) || (reinterpret_cast<uintptr_t>(ws) & 3u))
+    return KVC_EINVAL;
+  QuantJob job{x, codes, scales, gscale};
+  return cuda_status(launch_quant_fp4(&job, 1, n, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream) {
+  if (!c || !c->dev_ws) return KVC_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ECUDA;
+  int32_t w = 0;
+  if (cudaMemcpy(&w, c->dev_ws, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ECUDA;
+  if (w != 0) {
+    const int32_t z = 0;
+    if (cudaMemcpy(c->dev_ws, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return KVC_ECUDA;
+    return KVC_ETIMEOUT;
+  }
+  return KVC_OK;
+}
+
+int32_t kvc_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, kvc_stream_t stream) {
+  if (!dev_ws || limit_us < 1 || limit_us > 2000000) return KVC_EINVAL;
+  return cuda_status(launch_watchdog_selftest(dev_ws, limit_us, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* kvc_status_string(int32_t s) {
+  switch (s) {
+    case KVC_OK:
+      return "ok";
+    case KVC_EINVAL:
+      return "invalid argument";
+    case KVC_ESTATE:
+      return "invalid in the cache's current state";
+    case KVC_ECUDA:
+      return "CUDA error";
+    case KVC_ETIMEOUT:
+      return "device wait timed out";
+    case KVC_EUNSUPPORTED:
+      return "unsupported";
+    default:
+      return "unknown status";
+  }
+}
+
+}  // extern "C"

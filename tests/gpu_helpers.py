@@ -1,0 +1,33 @@
+"""Shared helpers for the GPU parity tests: tolerances and comparisons."""
+
+import numpy as np
+import torch
+
+# bf16 attention / recache against the float64 oracle
+ATOL_BF16 = 2e-2
+RELL2_BF16 = 5e-3
+# attention over an FP4 cache against the oracle run on the same dequantised K/V
+ATOL_FP4 = 5e-2
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def assert_close(got: np.ndarray, want: np.ndarray, atol: float, rel_l2: float | None, what: str):
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    mx = float(err.max()) if err.size else 0.0
+    msg = f"{what}: max-abs {mx:.3e} (tol {atol})"
+    if rel_l2 is not None:
+        den = float(np.linalg.norm(want))
+        rl = float(np.linalg.norm(got - want)) / den if den > 0 else float(np.linalg.norm(got))
+        msg += f", rel-L2 {rl:.3e} (tol {rel_l2})"
+        assert rl <= rel_l2, msg
+    assert mx <= atol, msg
+    return msg
+
+
+SAMPLE_ROWS_4680 = [0, 1, 63, 127, 128, 129, 200, 255, 256, 511, 1000, 1559, 1560, 2047, 2048,
+                    3119, 3120, 3333, 4095, 4096, 4500, 4607, 4608, 4650, 4679]

@@ -1,0 +1,213 @@
+"""GPU parity: cache append / evict / layout and bf16 sink+window attention,
+CUDA path (through the C ABI) against the float64 oracle on the same inputs."""
+
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle.cache_model import CacheModel, CacheStateError
+from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, bf16_to_f64
+from tests.gpu_helpers import (ATOL_BF16, RELL2_BF16, SAMPLE_ROWS_4680, assert_close, to64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def swl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sink_short_window_sinkwin_b300 as swl
+    return swl
+
+
+def _stream(swl, sh: Shapes, cfg: int, steps, dist="rms1", dtype="bf16", scrub=False,
+            check_every=True):
+    """Run chunks 0..steps-1 through GPU cache + oracle model; yields per step."""
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, dtype=dtype, scrub_on_evict=scrub)
+    model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    W = sh.window_chunks
+    for c in range(steps):
+        q, k, v = chunk_qkv(sh, cfg, 0, c, dist)
+        if c > W:
+            cache.evict(c - W)
+            model.evict(c - W)
+        cache.append(k.cuda(), v.cuda(), c)
+        model.append(c, bf16_to_f64(k), bf16_to_f64(v))
+        assert cache.chunk_of_region == model.chunk_of_region
+        yield c, q, cache, model
+
+
+def test_tiny_stream_layout_and_attention(swl):
+    sh = TINY
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    for c, q, cache, model in _stream(swl, sh, 0, 6, "rms1"):
+        Kp, Vp = model.physical()
+        got_k, got_v = to64(cache.k), to64(cache.v)
+        for r, ch in enumerate(model.chunk_of_region):
+            if ch >= 0:
+                sl = slice(r * sh.chunk_tokens, (r + 1) * sh.chunk_tokens)
+                assert np.array_equal(got_k[sl], Kp[sl]) and np.array_equal(got_v[sl], Vp[sl])
+        out = cache.attn(q.cuda(), scale)
+        torch.cuda.synchronize()
+        want = oatt.sinkwin_attention(model, bf16_to_f64(q), scale)
+        assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"tiny step {c}")
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+@pytest.mark.parametrize("dist", ["literal", "rms1"])
+def test_layer_attention_full_size(swl, dist):
+    """LongLive-1.3B layer, 12 x 128, chunk 4680, KV 18720; sampled query rows
+    across every tile kind (first, interior, slot 1, last partial)."""
+    sh = LAYER_1P3B
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    *_, (c, q, cache, model) = list(_stream(swl, sh, 1, 4, dist))
+    assert model.kv_length() == 18720
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    kk, vv = model.visible_kv()
+    want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, SAMPLE_ROWS_4680)
+    got = to64(out)[SAMPLE_ROWS_4680]
+    print(assert_close(got, want, ATOL_BF16, RELL2_BF16, f"layer {dist}"))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_layer_warmup_and_wrap(swl):
+    """KV lengths 4680, 9360, 14040 during warm-up and the ring after wrap-around
+    (step 5: regions hold chunks 0, 4, 5, 3)."""
+    sh = LAYER_1P3B
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    rows = [0, 130, 2500, 4679]
+    for c, q, cache, model in _stream(swl, sh, 1, 6, "rms1"):
+        if c in (0, 1, 2, 5):
+            out = cache.attn(q.cuda(), scale)
+            torch.cuda.synchronize()
+            kk, vv = model.visible_kv()
+            want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, rows)
+            assert_close(to64(out)[rows], want, ATOL_BF16, RELL2_BF16, f"step {c}")
+    assert model.chunk_of_region == [0, 4, 5, 3]
+
+
+@pytest.mark.parametrize("H,D,tpf,cf,W,tq", [
+    (2, 128, 100, 1, 3, 100),     # Tc = 100: every KV tile ragged
+    (3, 64, 50, 3, 2, 300),       # tq != Tc, slot 1 partly live
+    (1, 128, 16, 8, 2, 1),        # one query row
+    (2, 64, 129, 1, 4, 257),      # 129-row chunks, tq = 2*128 + 1
+    (1, 128, 200, 2, 1, 400),     # W = 1: sink + the current chunk only
+])
+def test_small_shapes_full_compare(swl, H, D, tpf, cf, W, tq):
+    sh = Shapes(H, D, tpf, cf, W, 1, tpf)
+    scale = 0.9 / math.sqrt(D)
+    for c, q, cache, model in _stream(swl, sh, 7, W + 3, "rms1"):
+        qq = chunk_qkv(sh, 8, 0, c, "rms1", q_rows=tq)[0]
+        out = cache.attn(qq.cuda(), scale)
+        torch.cuda.synchronize()
+        want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
+        assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"{(H, D, tpf, cf, W, tq)} step {c}")
+
+
+def test_holes_scrub_and_zero_queries(swl):
+    """Evict without append leaves a hole (two KV segments); the scrubbed slot
+    holds NaN and must never reach the output."""
+    sh = Shapes(2, 128, 100, 1, 3, 10, 10)
+    scale = 1.0 / math.sqrt(128)
+    gen = _stream(swl, sh, 9, 5, "rms1", scrub=True)
+    for c, q, cache, model in gen:
+        pass
+    cache.evict(2)
+    model.evict(2)
+    assert cache.chunk_of_region == [0, 4, -1, 3]
+    torch.cuda.synchronize()
+    assert torch.isnan(cache.k[200:300].float()).all() and torch.isnan(cache.v[200:300].float()).all()
+    qq = chunk_qkv(sh, 9, 1, 99, "rms1", q_rows=130)[0]
+    out = cache.attn(qq.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
+    assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, "hole")
+    # Q = 0 -> mean of the visible V (closed form)
+    z = torch.zeros((7, 2, 128), dtype=torch.bfloat16, device="cuda")
+    out0 = cache.attn(z, scale)
+    torch.cuda.synchronize()
+    _, vv = model.visible_kv()
+    assert_close(to64(out0), np.broadcast_to(vv.mean(axis=0), (7, 2, 128)), ATOL_BF16, None, "q=0")
+    # tq = 0 is a no-op
+    cache.attn(torch.zeros((0, 2, 128), dtype=torch.bfloat16, device="cuda"), scale)
+
+
+def test_evicted_data_does_not_influence_output(swl):
+    """Overwrite an evicted slot's rows with garbage: the output is bit-identical."""
+    sh = Shapes(2, 128, 100, 1, 3, 10, 10)
+    scale = 1.0 / math.sqrt(128)
+    for c, q, cache, model in _stream(swl, sh, 11, 5, "rms1"):
+        pass
+    cache.evict(2)
+    qq = chunk_qkv(sh, 11, 1, 5, "rms1", q_rows=100)[0].cuda()
+    a = cache.attn(qq, scale).clone()
+    cache.k[200:300].normal_()
+    cache.v[200:300].fill_(float("inf"))
+    b = cache.attn(qq, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_append_copy_is_exact_full_size(swl):
+    sh = LAYER_1P3B
+    for c, q, cache, model in _stream(swl, sh, 1, 4, "literal"):
+        pass
+    torch.cuda.synchronize()
+    for c in range(4):
+        _, k, v = chunk_qkv(sh, 1, 0, c, "literal")
+        sl = slice(c * sh.chunk_tokens, (c + 1) * sh.chunk_tokens)
+        assert torch.equal(cache.k[sl].cpu(), k) and torch.equal(cache.v[sl].cpu(), v)
+
+
+def test_state_machine_matches_oracle(swl):
+    """Random call sequences: the library and the oracle model accept and reject
+    the same calls and end in the same slot map."""
+    sh = Shapes(1, 64, 8, 2, 3, 2, 4)
+    rnd = random.Random(5)
+    z = torch.zeros((sh.chunk_tokens, 1, 64), dtype=torch.bfloat16, device="cuda")
+    zn = np.zeros((sh.chunk_tokens, 1, 64))
+    for trial in range(20):
+        cache = swl.KVCache(1, 64, 8, 2, 3)
+        model = CacheModel(1, 64, sh.chunk_tokens, 3)
+        for _ in range(40):
+            op = rnd.choice(["app_next", "app_same", "app_any", "evict_old", "evict_any"])
+            nw = model.newest()
+            if op == "app_next":
+                args = ("a", nw + 1)
+            elif op == "app_same":
+                args = ("a", max(nw, 0))
+            elif op == "app_any":
+                args = ("a", rnd.randint(0, nw + 3))
+            elif op == "evict_old":
+                win = [x for x in model.present_chunks() if x != 0]
+                args = ("e", win[0] if win else 0)
+            else:
+                args = ("e", rnd.randint(0, nw + 2))
+            try:
+                (model.append(args[1], zn, zn) if args[0] == "a" else model.evict(args[1]))
+                want = swl.KVC_OK
+            except CacheStateError:
+                want = swl.KVC_ESTATE
+            try:
+                (cache.append(z, z, args[1]) if args[0] == "a" else cache.evict(args[1]))
+                got = swl.KVC_OK
+            except swl.KvcError as e:
+                got = e.status
+            assert got == want, (trial, args)
+            assert cache.chunk_of_region == model.chunk_of_region
+
+
+def test_watchdog_reports_timeout(swl):
+    cache = swl.KVCache(1, 64, 16, 2, 2)
+    from sink_short_window_sinkwin_b300._abi import lib
+    import ctypes
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib().kvc_watchdog_selftest(ctypes.c_void_p(cache.ws.data_ptr()), 2000, st) == 0
+    assert cache.last_device_error() == swl.KVC_ETIMEOUT
+    assert cache.last_device_error() == swl.KVC_OK  # read-and-clear

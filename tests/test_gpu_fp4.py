@@ -1,0 +1,128 @@
+"""GPU parity of the FP4 KV path: codes, scales and tensor scales bit-exact
+against the oracle encoder; attention over an FP4 cache against the oracle run
+on the same dequantised K/V."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle import fp4 as ofp4
+from oracle.cache_model import CacheModel
+from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, bf16_to_f64
+from tests.gpu_helpers import ATOL_FP4, SAMPLE_ROWS_4680, assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def swl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sink_short_window_sinkwin_b300 as swl
+    return swl
+
+
+def _f32(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float32).numpy()
+
+
+def _check_quant(swl, x_bf16: torch.Tensor, what: str):
+    codes, scales, g = swl.quant_fp4(x_bf16.cuda().contiguous())
+    torch.cuda.synchronize()
+    wc, ws, wg = ofp4.quantize(_f32(x_bf16).reshape(-1, 16))
+    assert np.array_equal(codes.cpu().numpy(), wc.reshape(-1)), f"{what}: codes differ"
+    assert np.array_equal(scales.cpu().numpy(), ws.reshape(-1)), f"{what}: scales differ"
+    assert g.cpu().numpy()[0].view(np.uint32) == np.float32(wg).view(np.uint32), f"{what}: g differs"
+
+
+def test_quant_bitexact_layer_chunk(swl):
+    sh = LAYER_1P3B
+    _, k, v = chunk_qkv(sh, 3, 0, 0, "outliers")
+    _check_quant(swl, k, "K chunk")
+    _check_quant(swl, v, "V chunk")
+
+
+def test_quant_bitexact_edge_values(swl):
+    rng = np.random.default_rng(4)
+    blocks = []
+    blocks.append(np.zeros(16, np.float32))                       # all-zero block
+    blocks.append(np.full(16, -0.0, np.float32))                  # -0 only
+    b = np.zeros(16, np.float32); b[0] = 6.0; b[1:8] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    b[8:] = -b[:8]
+    blocks.append(b)                                              # E2M1 ties at s = 1
+    blocks.append(np.full(16, 3e-6, np.float32))                  # tiny: subnormal scales
+    blocks.append(rng.standard_normal(16).astype(np.float32) * 1e-3)
+    blocks.append(np.linspace(-448 * 6, 448 * 6, 16, dtype=np.float32))  # holds the amax
+    for _ in range(200):
+        blocks.append((rng.standard_normal(16) * np.exp(rng.uniform(-12, 4))).astype(np.float32))
+    x = torch.from_numpy(np.concatenate(blocks)).to(torch.bfloat16)
+    _check_quant(swl, x, "edge blocks")
+    _check_quant(swl, torch.zeros(64, dtype=torch.bfloat16), "all zero")
+    # many blocks: every CTA of both passes active, a grid-stride remainder
+    y = torch.from_numpy(rng.standard_normal(16 * 300001).astype(np.float32)).to(torch.bfloat16)
+    _check_quant(swl, y, "ragged size")
+
+
+def _fp4_stream(swl, sh, cfg, steps, dist):
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, dtype="fp4")
+    model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    W, Tc = sh.window_chunks, sh.chunk_tokens
+    enc = {}
+    for c in range(steps):
+        q, k, v = chunk_qkv(sh, cfg, 0, c, dist)
+        if c > W:
+            cache.evict(c - W)
+            model.evict(c - W)
+        cache.append(k.cuda(), v.cuda(), c)
+        ek = ofp4.quantize(_f32(k))
+        ev = ofp4.quantize(_f32(v))
+        enc[c] = (ek, ev)
+        model.append(c, ofp4.dequantize(*ek), ofp4.dequantize(*ev))
+        assert cache.chunk_of_region == model.chunk_of_region
+        torch.cuda.synchronize()
+        r = model.chunk_of_region.index(c)
+        sl = slice(r * Tc, (r + 1) * Tc)
+        for (codes, scales, g), cb, sb, gb in ((ek, cache.k, cache.k_scale, cache.k_gscale),
+                                              (ev, cache.v, cache.v_scale, cache.v_gscale)):
+            assert np.array_equal(cb[sl].cpu().numpy(), codes), f"codes of chunk {c}"
+            assert np.array_equal(sb[sl].cpu().numpy(), scales), f"scales of chunk {c}"
+            assert gb[r].item() == float(g), f"gscale of chunk {c}"
+        yield c, q, cache, model
+
+
+def test_fp4_tiny_stream(swl):
+    sh = TINY
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    for c, q, cache, model in _fp4_stream(swl, sh, 0, 6, "outliers"):
+        out = cache.attn(q.cuda(), scale)
+        torch.cuda.synchronize()
+        want = oatt.sinkwin_attention(model, bf16_to_f64(q), scale)
+        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 tiny step {c}")
+
+
+@pytest.mark.parametrize("H,D,tpf,cf,W,tq", [(2, 128, 100, 1, 3, 130), (3, 64, 50, 3, 2, 300)])
+def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
+    sh = Shapes(H, D, tpf, cf, W, 1, tpf)
+    scale = 1.0 / math.sqrt(D)
+    for c, q, cache, model in _fp4_stream(swl, sh, 5, W + 2, "outliers"):
+        qq = chunk_qkv(sh, 6, 0, c, "rms1", q_rows=tq)[0]
+        out = cache.attn(qq.cuda(), scale)
+        torch.cuda.synchronize()
+        want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
+        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 {(H, D, tpf, cf, W, tq)} step {c}")
+
+
+def test_fp4_layer_full_size(swl):
+    sh = LAYER_1P3B
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    *_, (c, q, cache, model) = list(_fp4_stream(swl, sh, 3, 4, "outliers"))
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    kk, vv = model.visible_kv()
+    want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, SAMPLE_ROWS_4680)
+    print(assert_close(to64(out)[SAMPLE_ROWS_4680], want, ATOL_FP4, None, "fp4 layer"))
+    assert cache.last_device_error() == swl.KVC_OK

@@ -1,0 +1,123 @@
+"""GPU parity of the prompt-switch KV recache (projection GEMM + RMSNorm + 3D
+RoPE written into the cache), then attention over the rebuilt cache."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle import recache as orc
+from oracle.cache_model import CacheModel
+from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, recache_inputs, bf16_to_f64
+from tests.gpu_helpers import ATOL_BF16, RELL2_BF16, SAMPLE_ROWS_4680, assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def swl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sink_short_window_sinkwin_b300 as swl
+    return swl
+
+
+def _fill(swl, sh: Shapes, upto: int):
+    """Cache + oracle model holding the chunks present after streaming 0..upto
+    (zero K/V: the recache overwrites them)."""
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, sh.window_chunks)
+    model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    z = torch.zeros((sh.chunk_tokens, sh.heads, sh.head_dim), dtype=torch.bfloat16, device="cuda")
+    zn = np.zeros((sh.chunk_tokens, sh.heads, sh.head_dim))
+    for c in range(upto + 1):
+        if c > sh.window_chunks:
+            cache.evict(c - sh.window_chunks)
+            model.evict(c - sh.window_chunks)
+        cache.append(z, z, c)
+        model.append(c, zn, zn)
+    return cache, model
+
+
+def _recache_both(swl, sh, cache, model, cfg, gamma_rand=False):
+    ids = model.present_chunks()
+    hid, wkv, gamma = recache_inputs(sh, cfg, len(ids))
+    if gamma_rand:
+        g = np.random.default_rng(cfg).uniform(0.5, 1.5, sh.model_dim).astype(np.float32)
+        gamma = torch.from_numpy(g)
+    cache.recache(hid.cuda(), wkv.cuda(), gamma.cuda(), ids, sh.grid_h, sh.grid_w)
+    k, v = orc.recache(bf16_to_f64(hid), bf16_to_f64(wkv), gamma.double().numpy(), ids,
+                       sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, sh.grid_w)
+    model.recache(ids, k, v)
+    torch.cuda.synchronize()
+    return ids
+
+
+def _compare_cache(cache, model, sh, rows=None, what=""):
+    Kp, Vp = model.physical(fill=0.0)
+    gk, gv = to64(cache.k), to64(cache.v)
+    for r, ch in enumerate(model.chunk_of_region):
+        if ch < 0:
+            continue
+        base = r * sh.chunk_tokens
+        sel = np.arange(sh.chunk_tokens) if rows is None else np.asarray(rows)
+        assert_close(gk[base + sel], Kp[base + sel], ATOL_BF16, RELL2_BF16, f"{what} K region {r}")
+        assert_close(gv[base + sel], Vp[base + sel], ATOL_BF16, RELL2_BF16, f"{what} V region {r}")
+
+
+def test_recache_tiny_then_attention(swl):
+    sh = TINY
+    cache, model = _fill(swl, sh, 4)  # present: 0, 3, 4
+    assert model.present_chunks() == [0, 3, 4]
+    _recache_both(swl, sh, cache, model, 4, gamma_rand=True)
+    _compare_cache(cache, model, sh, what="tiny")
+    q = chunk_qkv(sh, 4, 0, 5, "rms1")[0]
+    out = cache.attn(q.cuda(), 0.125)
+    torch.cuda.synchronize()
+    assert_close(to64(out), oatt.sinkwin_attention(model, bf16_to_f64(q), 0.125),
+                 ATOL_BF16, RELL2_BF16, "tiny attention after recache")
+
+
+def test_recache_cluster_noncontiguous_positions(swl):
+    """H*D = 512: a 2-CTA cluster shares the RMSNorm sums; chunks {0, 97, 98, 99}
+    put frame positions far apart (294..299 next to 0..2)."""
+    sh = Shapes(4, 128, 60, 3, 3, 6, 10)
+    cache, model = _fill(swl, sh, 99)
+    assert model.present_chunks() == [0, 97, 98, 99]
+    _recache_both(swl, sh, cache, model, 44)
+    _compare_cache(cache, model, sh, what="cluster")
+
+
+def test_recache_layer_full_size_then_attention(swl):
+    """Prompt switch before chunk 4: chunks {0,1,2,3} = 12 frames, 18720 x 1536
+    hidden states, then one 4680-query attention step over the rebuilt cache."""
+    sh = LAYER_1P3B
+    cache, model = _fill(swl, sh, 3)
+    _recache_both(swl, sh, cache, model, 4)
+    rows = [0, 1, 51, 52, 127, 128, 1559, 1560, 3000, 4607, 4608, 4679]
+    _compare_cache(cache, model, sh, rows=rows, what="layer")
+    q = chunk_qkv(sh, 4, 0, 4, "rms1")[0]
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    kk, vv = model.visible_kv()
+    want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, SAMPLE_ROWS_4680)
+    print(assert_close(to64(out)[SAMPLE_ROWS_4680], want, ATOL_BF16, RELL2_BF16,
+                       "attention after layer recache"))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_recache_rejections(swl):
+    sh = TINY
+    cache, model = _fill(swl, sh, 2)
+    hid, wkv, gamma = recache_inputs(sh, 0, 3)
+    with pytest.raises(swl.KvcError) as e:
+        cache.recache(hid.cuda(), wkv.cuda(), None, [0, 2, 1], sh.grid_h, sh.grid_w)
+    assert e.value.status == swl.KVC_ESTATE
+    f = swl.KVCache(1, 64, 16, 2, 2, dtype="fp4")
+    z = torch.zeros((32, 1, 64), dtype=torch.bfloat16, device="cuda")
+    f.append(z, z, 0)
+    with pytest.raises(swl.KvcError) as e:
+        f.recache(hid[:32].cuda(), wkv.cuda(), None, [0], 4, 4)
+    assert e.value.status == swl.KVC_EUNSUPPORTED
