@@ -122,8 +122,8 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
 /* out = softmax(softmax_scale * q K^T) V per head, over the visible keys: the
  * sink region plus every occupied window slot (no mask inside that set; keys are
  * read in physical order, which softmax does not see).  q, out: device bf16
- * [tq][H][D]; tq >= 0 (0 is a no-op).  FP4 caches are dequantised inside the tile
- * load.  Attention supports D in {64, 128} (else KVC_EUNSUPPORTED); the sink
+ * [tq][H][D]; tq >= 0 (0 is a no-op); softmax_scale finite and >= 0 (else
+ * KVC_EINVAL).  FP4 caches are dequantised inside the tile load.  Attention supports D in {64, 128} (else KVC_EUNSUPPORTED); the sink
  * must be present (else KVC_ESTATE).  A kernel wait that runs out leaves
  * KVC_ETIMEOUT for kvc_last_device_error. */
 int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,

@@ -540,7 +540,10 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   p.kg = a.k_gscale;
   p.vg = a.v_gscale;
   p.Tc = a.chunk_tokens;
-  const size_t smem = sizeof(AttnSmem<D>) + 1024;
+  // one CTA per SM: a second resident CTA would wait in tcgen05.alloc for the
+  // 512 TMEM columns the first one holds
+  size_t smem = sizeof(AttnSmem<D>) + 1024;
+  if (smem < 120 * 1024) smem = 120 * 1024;
   auto kern = sinkwin_attn_kernel<D, kFp4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -273,7 +273,8 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, f
                      kvc_stream_t stream) {
   if (!ready(c) || tq < 0) return KVC_EINVAL;
   if (tq == 0) return KVC_OK;
-  if (!q || !out || !aligned16(q) || !aligned16(out) || !std::isfinite(softmax_scale))
+  if (!q || !out || !aligned16(q) || !aligned16(out) || !std::isfinite(softmax_scale) ||
+      softmax_scale < 0.0f)
     return KVC_EINVAL;
   if (c->head_dim != 64 && c->head_dim != 128) return KVC_EUNSUPPORTED;
   if (c->chunk_of_region[0] != 0) return KVC_ESTATE;

@@ -97,6 +97,7 @@ def test_rejections_change_nothing(lib):
     assert lib.sinkwin_attn(ctypes.byref(c), q, q, -1, 0.125, s) == _abi.KVC_EINVAL
     assert lib.sinkwin_attn(ctypes.byref(c), q, q, 0, 0.125, s) == _abi.KVC_OK  # empty: no-op
     assert lib.sinkwin_attn(ctypes.byref(c), q, q, 8, float("nan"), s) == _abi.KVC_EINVAL
+    assert lib.sinkwin_attn(ctypes.byref(c), q, q, 8, -0.125, s) == _abi.KVC_EINVAL
     ids = (ctypes.c_int64 * 1)(0)
     assert lib.kvc_recache(ctypes.byref(c), q, q, None, 1e-6, ids, 1, 4, 4, 1e4, s) == _abi.KVC_ESTATE
     assert lib.kvc_recache(ctypes.byref(c), q, q, None, 1e-6, ids, 1, 3, 4, 1e4, s) == _abi.KVC_EINVAL
