@@ -159,12 +159,18 @@ def _blas_threads():
         return 1
 
 
+def _cores():
+    """Threads the oracle runs on: its matmuls use the BLAS pool, the einsum
+    and elementwise parts one thread."""
+    return min(len(os.sched_getaffinity(0)), _blas_threads())
+
+
 def cpu_baseline(target_s: float = 12.0):
     dt, _ = cpu_sample(8)
     rows = int(max(8, min(TC, 8 * target_s / max(dt, 1e-3))))
     dt, flop = cpu_sample(rows, seed=1)
-    cores = min(len(os.sched_getaffinity(0)), _blas_threads())
-    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "host_cpus": len(os.sched_getaffinity(0)), "blas_threads": _blas_threads(),
             "sample": f"{rows} of 4680 query rows of both attentions (18720 keys, 12 heads), "
                       f"{4 * rows} of 18720 recache rows, FP4 encode of {rows} rows; "
                       f"{dt:.1f} s float64 numpy"}
@@ -186,7 +192,7 @@ def run_reference(args):
         times.append(dt)
     mean = sum(times) / len(times)
     value = flop / mean / 1e12
-    cores = min(len(os.sched_getaffinity(0)), _blas_threads())
+    cores = _cores()
     sample = (f"{rows} of 4680 query rows of both attentions, {4 * rows} recache rows, "
               f"FP4 encode of {rows} rows per step")
     print(json.dumps({
@@ -210,6 +216,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=NLAYERS,
+                    help="independent layer caches the steps rotate over (fewer: smaller "
+                         "device footprint, e.g. for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -239,7 +248,8 @@ def main():
     wkv = randn((HD, 2 * HD), 0.02)
     gamma = torch.ones(HD, dtype=torch.float32, device=dev)
     layers = []
-    for li in range(NLAYERS):
+    nlayers = max(1, args.layers)
+    for li in range(nlayers):
         L = {
             "bf": swl.KVCache(H, D, TPF, CF, W, dtype="bf16", device=dev),
             "f4": swl.KVCache(H, D, TPF, CF, W, dtype="fp4", device=dev),
@@ -280,10 +290,12 @@ def main():
                 evs[i + 1].record()
         L["c"] = c
 
-    launches_per_step = 1 + 1 + 1 + 2 + 1  # recache, copy, attn, amax+quant, attn
+    # recache (K GEMM, norm+RoPE, V GEMM), bf16 append copy, bf16 attention,
+    # FP4 append (amax, encode), FP4 attention; evict without scrub launches nothing
+    launches_per_step = 3 + 1 + 1 + 2 + 1
 
     for i in range(args.warmup):
-        step(layers[i % NLAYERS])
+        step(layers[i % nlayers])
     torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
@@ -297,7 +309,7 @@ def main():
     time.sleep(0.3)  # let the sampler take a first reading
     t_wall = time.perf_counter()
     for s in range(args.steps):
-        step(layers[(args.warmup + s) % NLAYERS], ev[s])
+        step(layers[(args.warmup + s) % nlayers], ev[s])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if dist:
@@ -330,7 +342,7 @@ def main():
     torch.cuda.synchronize()
     e_start.record()
     for s in range(n_e2e):
-        L = layers[s % NLAYERS]
+        L = layers[s % nlayers]
         for n in ("q", "k", "v", "k4", "v4", "hid"):
             L[n].copy_(host[n], non_blocking=True)
         wkv.copy_(host["wkv"], non_blocking=True)
@@ -392,7 +404,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "step": "recache + (evict, append, attention) on a bf16 "
                    "cache + (evict, FP4 append, attention) on an FP4 cache",
-                   "step_gflop": STEP_FLOP / 1e9, "layers_rotated": NLAYERS,
+                   "step_gflop": STEP_FLOP / 1e9, "layers_rotated": nlayers,
                    "l2": "inputs larger than L2: 8 rotating layer caches, >300 MB touched per step",
                    "parallelism": f"replicas x{world}"},
         "latent_frames_per_s_per_layer": CF / (chunk_step_ms * 1e-3),

@@ -88,6 +88,7 @@ typedef struct kvc_cache {
   /* ---- library-maintained state: read-only for the caller ---- */
   int32_t init_magic;
   int64_t chunk_of_region[1 + KVC_MAX_WINDOW]; /* -1 = empty */
+  int64_t last_chunk;                          /* highest chunk appended so far, -1 = none */
 } kvc_cache;
 
 /* sizeof(kvc_cache) as compiled into the library (lets bindings check the layout). */
@@ -105,9 +106,9 @@ int32_t kvc_init(kvc_cache* c);
 /* Append chunk `chunk_idx`: k_chunk, v_chunk are device bf16 [Tc][H][D]
  * (post-norm, post-RoPE keys, as the layer produced them).  The sink is chunk 0;
  * chunk c >= 1 goes to ring slot (c-1) % W.  Allowed: chunk 0 into an empty
- * cache; the newest chunk again (overwrite, one call per denoise step); the next
- * chunk once its slot is empty (evict the oldest window chunk first).  Else
- * KVC_ESTATE.  bf16 cache: a 128-bit vectorised copy.  FP4 cache: the chunk's K
+ * cache; the last appended chunk again while it is still cached (overwrite, one
+ * call per denoise step); chunk last_chunk + 1 once its slot is empty (evict the
+ * oldest window chunk first).  Else KVC_ESTATE.  bf16 cache: a 128-bit vectorised copy.  FP4 cache: the chunk's K
  * and V are quantised (tensor amax -> fp32 gscale[region], E4M3 block scales,
  * E2M1 codes; the encode rule is kvc_quant_fp4's). */
 int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
@@ -141,7 +142,11 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
  * t % grid_w (grid_h * grid_w == tokens_per_frame); the D/2 rotation pairs
  * (adjacent elements) are split into [frame | row | column] bands of
  * (P - 2*(P/3), P/3, P/3) pairs, P = D/2; in a band of b dims pair j turns by
- * position * rope_theta^(-2j/b).  bf16 caches only (FP4: KVC_EUNSUPPORTED). */
+ * position * rope_theta^(-2j/b).  bf16 caches only (FP4: KVC_EUNSUPPORTED);
+ * H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} (else KVC_EUNSUPPORTED).
+ * Runs as three launches on `stream` (K projection, norm + RoPE, V projection);
+ * between them the regions being rebuilt hold intermediate values, so nothing
+ * may read those regions until the stream passes the call. */
 int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const float* gamma_k,
                     float eps, const int64_t* chunk_ids, int32_t n, int32_t grid_h,
                     int32_t grid_w, float rope_theta, kvc_stream_t stream);

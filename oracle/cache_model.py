@@ -13,9 +13,11 @@ Readings (the pages leave them open):
   (c-1) mod W, i.e. region 1 + (c-1) mod W, rows [region*Tc, (region+1)*Tc);
 * the window's W slots include the chunk currently being generated, so the
   visible set of chunk c is {0} U {max(1, c-W+1) .. c};
-* a chunk is appended only when its slot is empty or already holds it
-  (re-appending the newest chunk overwrites it: one call per denoise step);
-  the caller evicts the oldest window chunk first; the sink is never evicted.
+* chunks arrive in order: the next chunk is the one after the last appended
+  (whether or not that one is still cached), and it needs an empty slot, so the
+  caller evicts the oldest window chunk first; re-appending the last chunk while
+  it is cached overwrites it (one call per denoise step); the sink is never
+  evicted.
 """
 
 from __future__ import annotations
@@ -44,6 +46,7 @@ class CacheModel:
     def __init__(self, heads: int, head_dim: int, chunk_tokens: int, window_chunks: int):
         self.H, self.D, self.Tc, self.W = heads, head_dim, chunk_tokens, window_chunks
         self.chunk_of_region = [-1] * (1 + window_chunks)
+        self.last = -1  # highest chunk appended so far
         self.k: dict[int, np.ndarray] = {}
         self.v: dict[int, np.ndarray] = {}
 
@@ -66,17 +69,14 @@ class CacheModel:
             raise ValueError("negative chunk index")
         if k.shape != (self.Tc, self.H, self.D) or v.shape != k.shape:
             raise ValueError("chunk shape mismatch")
-        if self.chunk_of_region[0] != 0:
-            if c != 0:
-                raise CacheStateError("the sink (chunk 0) must be appended first")
-        else:
-            nw = self.newest()
-            if c not in (nw, nw + 1):
-                raise CacheStateError("only the newest chunk or the next one may be appended")
         r = region_of_chunk(c, self.W)
-        if self.chunk_of_region[r] not in (-1, c):
-            raise CacheStateError("slot still holds an older chunk: evict it first")
+        if c == self.last + 1:
+            if self.chunk_of_region[r] != -1:
+                raise CacheStateError("slot still holds an older chunk: evict it first")
+        elif not (c == self.last and self.chunk_of_region[r] == c):
+            raise CacheStateError("only the next chunk, or the last one while cached, may be appended")
         self.chunk_of_region[r] = c
+        self.last = c
         self.k[c] = np.array(k, dtype=np.float64, copy=True)
         self.v[c] = np.array(v, dtype=np.float64, copy=True)
 

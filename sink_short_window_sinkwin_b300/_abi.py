@@ -34,6 +34,7 @@ class KvcCache(ctypes.Structure):
         ("k_gscale", _vp), ("v_gscale", _vp), ("dev_ws", _vp),
         ("scrub_on_evict", _i32), ("init_magic", _i32),
         ("chunk_of_region", _i64 * (1 + KVC_MAX_WINDOW)),
+        ("last_chunk", _i64),
     ]
 
 

@@ -76,6 +76,8 @@ struct RecacheLaunch {
   int32_t* dev_err;
 };
 cudaError_t launch_recache(const RecacheLaunch& r, cudaStream_t st);
+// H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} and D even, D/2 <= 128
+bool recache_supported(int H, int D);
 
 // ---- diagnostics ----
 cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st);

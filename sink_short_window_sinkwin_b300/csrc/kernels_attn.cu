@@ -100,11 +100,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-template <int D>
+// Exact partial decode e2m1(code) * e4m3(scale): at most 6 significant bits
+// and a range of [2^-10, 2688], so the product is exact in f16 and in bf16.
+// The fp32 tensor scale of the region is applied by the softmax instead (K: in
+// the logit scale, V: folded into P), so no tile value is rounded here.
+template <int D, bool kHalfOut>
 __device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r, int grow,
                                             bool live, const uint8_t* codes, const uint8_t* scales,
-                                            const float* gsc, const AttnParams& p, int h) {
-  constexpr int DB = D / 64;
+                                            const AttnParams& p, int h) {
   uint8_t* base = reinterpret_cast<uint8_t*>(dst);
   if (!live) {
 #pragma unroll
@@ -115,7 +118,6 @@ __device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r
     }
     return;
   }
-  const float g = gsc[grow / p.Tc];
   const uint8_t* crow = codes + ((size_t)grow * p.H + h) * (D / 2);
   const uint8_t* srow = scales + ((size_t)grow * p.H + h) * (D / 16);
   uint32_t sc[D / 16];
@@ -135,15 +137,19 @@ __device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r
     const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // one 16-element block -> two 16-byte chunks
-      const float f = e4m3_to_f32(sc[q16 * 2 + half]) * g;
+      const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc[q16 * 2 + half]));  // exact
       uint32_t outw[8];
 #pragma unroll
       for (int bi = 0; bi < 8; ++bi) {
         const uint32_t word = w[half * 2 + (bi >> 2)];
         const uint32_t h2 = e2m1x2_to_f16x2((word >> (8 * (bi & 3))) & 0xFFu);
-        const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-        const float2 fv = __half22float2(hv);
-        outw[bi] = pack_bf16x2(fv.x * f, fv.y * f);
+        const __half2 hv = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);  // exact
+        if constexpr (kHalfOut) {
+          outw[bi] = *reinterpret_cast<const uint32_t*>(&hv);
+        } else {
+          const float2 fv = __half22float2(hv);
+          outw[bi] = pack_bf16x2(fv.x, fv.y);  // exact
+        }
       }
       const int e0 = q16 * 32 + half * 16;  // first element of this block
 #pragma unroll
@@ -260,11 +266,11 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       const int grow = cur.row0(p) + r;
       const bool live = r < cur.valid(p);
       if (t >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) break;
-      dequant_row<D>(sm.k[st], r, grow, live, p.kc, p.ks, p.kg, p, h);
+      dequant_row<D, false>(sm.k[st], r, grow, live, p.kc, p.ks, p, h);
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_kfull[st]);
       if (t >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) break;
-      dequant_row<D>(sm.v[st], r, grow, live, p.vc, p.vs, p.vg, p, h);
+      dequant_row<D, true>(sm.v[st], r, grow, live, p.vc, p.vs, p, h);
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_vfull[st]);
       cur.next(p);
@@ -273,7 +279,9 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+      // FP4 cache: P (scaled by the V tensor scale) and V' are f16
+      constexpr uint32_t idesc_pv =
+          kFp4 ? idesc_f16_f32(BM, D, false, true) : idesc_bf16_f32(BM, D, false, true);
       const uint32_t tS[2] = {tmem, tmem + 256};
       const uint32_t tO[2] = {tmem + 128, tmem + 384};
       auto qk = [&](int slot, int st) {
@@ -375,7 +383,8 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       };
       KvCursor cur;
       for (int t = 0; t < nt; ++t) {
-        if (!mbar_wait(&sm.bar_s[slot], t & 1, wd)) {
+        // warp-uniform exit: the tcgen05.ld/st below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], t & 1, wd))) {
           ok = false;
           break;
         }
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           // key rows past the segment end may hold anything (NaN scrub,
           // never-written memory): zero them in the V stage before P*V
           const int st = t & 1;
-          if (!mbar_wait(&sm.bar_vfull[st], (t >> 1) & 1, wd)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_vfull[st], (t >> 1) & 1, wd))) {
             ok = false;
             break;
           }
@@ -428,7 +437,12 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           }
           l += sum;
         } else {
-          // two passes over 32-column chunks (fewer live registers)
+          // two passes over 32-column chunks (fewer live registers).  The tile
+          // lies in one region: its K tensor scale joins the logit scale, its
+          // V tensor scale multiplies P (stored as f16 for the f16 P*V MMA)
+          const int region = p.seg[cur.seg].row0 / p.Tc;
+          const float cg = c * p.kg[region];
+          const float gv = p.vg[region];
           float mx = -INFINITY;
 #pragma unroll
           for (int j = 0; j < BN / 32; ++j) {
@@ -439,7 +453,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
             for (int e = 0; e < 32; ++e)
               if (j * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(sr[e]));
           }
-          rescale_if_needed(t, mx * c, m_ref, l, tO);
+          rescale_if_needed(t, mx * cg, m_ref, l, tO);
           const float neg = -m_ref;
           float sum = 0.0f;
 #pragma unroll
@@ -453,11 +467,11 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int k0 = j * 32 + 2 * e;
-              const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e]), c, neg)) : 0.0f;
+              const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e]), cg, neg)) : 0.0f;
               const float p1 =
-                  k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), c, neg)) : 0.0f;
+                  k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), cg, neg)) : 0.0f;
               sum += p0 + p1;
-              pk[e] = pack_bf16x2(p0, p1);
+              pk[e] = pack_f16x2(p0 * gv, p1 * gv);
             }
             tmem_st16(tS + j * 16, pk);
           }
@@ -468,7 +482,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
         mbar_arrive(&sm.bar_p[slot]);
         cur.next(p);
       }
-      if (ok && mbar_wait(&sm.bar_s[slot], nt & 1, wd)) {
+      if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], nt & 1, wd))) {
         tc_fence_after();
         const int grow = m0 + slot * BM + row;
         const float inv_l = 1.0f / l;

@@ -115,12 +115,6 @@ bool ready(const kvc_cache* c) { return c && c->init_magic == KVC_INIT_MAGIC && 
 
 int32_t region_of(int64_t chunk, int32_t W) { return chunk == 0 ? 0 : 1 + (int32_t)((chunk - 1) % W); }
 
-int64_t newest_chunk(const kvc_cache* c) {
-  int64_t m = -1;
-  for (int r = 0; r <= c->window_chunks; ++r) m = c->chunk_of_region[r] > m ? c->chunk_of_region[r] : m;
-  return m;
-}
-
 int64_t oldest_window_chunk(const kvc_cache* c) {
   int64_t m = -1;
   for (int r = 1; r <= c->window_chunks; ++r) {
@@ -200,6 +194,7 @@ int32_t kvc_init(kvc_cache* c) {
       return KVC_EINVAL;
   }
   for (int r = 0; r < 1 + KVC_MAX_WINDOW; ++r) c->chunk_of_region[r] = -1;
+  c->last_chunk = -1;
   c->init_magic = KVC_INIT_MAGIC;
   return KVC_OK;
 }
@@ -208,16 +203,14 @@ int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64
                    kvc_stream_t stream) {
   if (!ready(c) || !k_chunk || !v_chunk || !aligned16(k_chunk) || !aligned16(v_chunk) || chunk_idx < 0)
     return KVC_EINVAL;
-  // state
-  if (c->chunk_of_region[0] != 0) {
-    if (chunk_idx != 0) return KVC_ESTATE;
-  } else {
-    const int64_t nw = newest_chunk(c);
-    if (chunk_idx != nw && chunk_idx != nw + 1) return KVC_ESTATE;
-  }
+  // state: the next chunk, or the last one again while it is still cached
   const int32_t r = region_of(chunk_idx, c->window_chunks);
   const int64_t occ = c->chunk_of_region[r];
-  if (occ != -1 && occ != chunk_idx) return KVC_ESTATE;
+  if (chunk_idx == c->last_chunk + 1) {
+    if (occ != -1) return KVC_ESTATE;  // the slot still holds an older chunk
+  } else if (!(chunk_idx == c->last_chunk && occ == chunk_idx)) {
+    return KVC_ESTATE;
+  }
   // launch
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t Tc = chunk_tokens(c);
@@ -237,6 +230,7 @@ int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64
   }
   if (e != cudaSuccess) return KVC_ECUDA;
   c->chunk_of_region[r] = chunk_idx;
+  c->last_chunk = chunk_idx;
   return KVC_OK;
 }
 
@@ -291,7 +285,9 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, f
   for (int r = 0; r <= c->window_chunks; ++r) {
     if (c->chunk_of_region[r] < 0) continue;
     const int32_t row0 = r * Tc;
-    if (a.nseg > 0 && a.seg[a.nseg - 1].row0 + a.seg[a.nseg - 1].rows == row0)
+    // bf16: adjacent regions merge into one run of keys.  FP4: one segment per
+    // region, so every K/V tile has a single pair of tensor scales.
+    if (c->dtype == KVC_BF16 && a.nseg > 0 && a.seg[a.nseg - 1].row0 + a.seg[a.nseg - 1].rows == row0)
       a.seg[a.nseg - 1].rows += Tc;
     else
       a.seg[a.nseg++] = Seg{row0, Tc};
@@ -319,11 +315,7 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
   if (!(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta > 0.0f) || !std::isfinite(rope_theta))
     return KVC_EINVAL;
   if (c->dtype != KVC_BF16) return KVC_EUNSUPPORTED;
-  const int HD = c->heads * c->head_dim;
-  if (!((HD % 256 == 0 && HD / 256 <= 8) || (HD % 128 == 0 && HD / 128 <= 8) ||
-        (HD % 64 == 0 && HD / 64 <= 8)))
-    return KVC_EUNSUPPORTED;
-  if (c->head_dim / 2 > 128) return KVC_EUNSUPPORTED;
+  if (!recache_supported(c->heads, c->head_dim)) return KVC_EUNSUPPORTED;
   int64_t present[1 + KVC_MAX_WINDOW];
   const int np = present_chunks(c, present);
   if (np != n) return KVC_ESTATE;

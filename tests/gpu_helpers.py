@@ -20,6 +20,11 @@ def assert_close(got: np.ndarray, want: np.ndarray, atol: float, rel_l2: float |
     err = np.abs(got - want)
     mx = float(err.max()) if err.size else 0.0
     msg = f"{what}: max-abs {mx:.3e} (tol {atol})"
+    if err.size and mx > atol:
+        idx = np.unravel_index(int(np.argmax(err)), err.shape)
+        bad = np.argwhere(err > atol)
+        msg += (f" at {tuple(int(i) for i in idx)} got {got[idx]:.5f} want {want[idx]:.5f};"
+                f" {len(bad)} elements over, first {bad[:3].tolist()} last {bad[-3:].tolist()}")
     if rel_l2 is not None:
         den = float(np.linalg.norm(want))
         rl = float(np.linalg.norm(got - want)) / den if den > 0 else float(np.linalg.norm(got))

@@ -79,14 +79,16 @@ def test_recache_tiny_then_attention(swl):
                  ATOL_BF16, RELL2_BF16, "tiny attention after recache")
 
 
-def test_recache_cluster_noncontiguous_positions(swl):
-    """H*D = 512: a 2-CTA cluster shares the RMSNorm sums; chunks {0, 97, 98, 99}
-    put frame positions far apart (294..299 next to 0..2)."""
+def test_recache_two_column_tiles_noncontiguous_positions(swl):
+    """H*D = 512: the K row spans two 256-wide GEMM tiles, so the RMSNorm needs
+    the whole parked fp32 row; 180-token chunks make row tiles straddle chunks,
+    and chunks {0, 97, 98, 99} put frame positions far apart (294..299 next to
+    0..2)."""
     sh = Shapes(4, 128, 60, 3, 3, 6, 10)
     cache, model = _fill(swl, sh, 99)
     assert model.present_chunks() == [0, 97, 98, 99]
     _recache_both(swl, sh, cache, model, 44)
-    _compare_cache(cache, model, sh, what="cluster")
+    _compare_cache(cache, model, sh, what="two tiles")
 
 
 def test_recache_layer_full_size_then_attention(swl):

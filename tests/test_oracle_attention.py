@@ -218,3 +218,22 @@ def test_state_errors():
         m.recache([0, 3, 2], np.zeros((6, 1, 16)), np.zeros((6, 1, 16)))
     m.recache([0, 2, 3], np.ones((6, 1, 16)), np.ones((6, 1, 16)))
     assert m.k[3][0, 0, 0] == 1.0
+
+
+def test_window_of_one_chunk_streams():
+    """W = 1: the window holds only the current chunk; evicting it empties the
+    window and the next chunk still follows the last one appended."""
+    m = CacheModel(1, 16, 2, 1)
+    z = np.zeros((2, 1, 16))
+    m.append(0, z, z)
+    for c in range(1, 6):
+        if c > 1:
+            with pytest.raises(CacheStateError):
+                m.append(c, z, z)  # slot still holds c - 1
+            m.evict(c - 1)
+            with pytest.raises(CacheStateError):
+                m.append(c - 1, z, z)  # evicted: cannot come back
+        m.append(c, z, z)
+        m.append(c, z, z)  # overwrite while cached
+        assert m.chunk_of_region == [0, c]
+        assert m.present_chunks() == visible_chunks_of_step(c, 1)
