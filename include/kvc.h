@@ -163,6 +163,26 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
 int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, float* gscale,
                       int32_t* ws, kvc_stream_t stream);
 
+/* kvc_quant_fp4 without caller scratch.  The pages have no counterpart to
+ * this call: it exists for callers that cannot allocate device memory when they
+ * encode -- e.g. a host program whose device memory is all owned by another
+ * allocator, or a latency-critical loop where a cudaMalloc (which may
+ * synchronise the device) is not allowed.  Same arguments, encode rule and
+ * outputs as kvc_quant_fp4 minus `ws`; the library allocates nothing.
+ * Scratch: a static device array of KVC_NOALLOC_SCRATCH_WORDS int32 (1 KiB)
+ * inside the library, held by every GPU that loads it until the process exits.
+ * Its device address is looked up on the first call on each device (with that
+ * device current), so make that first call before any stream capture.  All
+ * calls share the array: calls that overlap on the GPU (other streams, other
+ * threads) race and must be ordered by the caller.  Nothing in it has to start
+ * at zero: each call's first pass writes every word its second pass reads.
+ * Uses the current device.  n must be a multiple of 16 in [16,
+ * KVC_NOALLOC_MAX_ELEMS], else KVC_EINVAL. */
+#define KVC_NOALLOC_SCRATCH_WORDS 256
+#define KVC_NOALLOC_MAX_ELEMS (((int64_t)1) << 35)
+int32_t kvc_quant_fp4_noalloc(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
+                              float* gscale, kvc_stream_t stream);
+
 /* Synchronise `stream`, read and clear the cache's device error word.
  * KVC_OK, KVC_ETIMEOUT (a kernel wait ran out), or KVC_ECUDA (a sticky CUDA error). */
 int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream);
