@@ -83,6 +83,12 @@ typedef struct kvc_cache {
   float* v_gscale;   /* FP4 only, [1 + W], else NULL */
   int32_t* dev_ws;   /* KVC_WS_WORDS int32, zero-filled by the caller before kvc_init;
                         word 0 is the device error word, the rest is reduction scratch */
+  void* attn_ws;     /* optional attention workspace of kvc_cache_bytes(c, 7) bytes,
+                        zero-filled by the caller before first use, or NULL.  With it
+                        sinkwin_attn balances work evenly over all SMs (items cut at a
+                        CTA boundary are merged through it); without it every CTA
+                        takes whole items.  Calls sharing it must be stream-ordered. */
+  uint64_t attn_ws_bytes; /* its size in bytes */
   /* ---- options ---- */
   int32_t scrub_on_evict; /* nonzero: kvc_evict overwrites the freed slot with NaN */
   /* ---- library-maintained state: read-only for the caller ---- */
@@ -95,7 +101,8 @@ typedef struct kvc_cache {
 size_t kvc_sizeof_cache(void);
 
 /* Bytes of one device buffer of a cache with this geometry.
- * which: 0 k, 1 v, 2 k_scale, 3 v_scale, 4 k_gscale, 5 v_gscale, 6 dev_ws.
+ * which: 0 k, 1 v, 2 k_scale, 3 v_scale, 4 k_gscale, 5 v_gscale, 6 dev_ws,
+ * 7 attn_ws (depends on the SM count of the current device; 0 without one).
  * Returns 0 for a buffer the dtype does not use or for an invalid geometry. */
 size_t kvc_cache_bytes(const kvc_cache* c, int32_t which);
 

@@ -32,6 +32,7 @@ class KvcCache(ctypes.Structure):
         ("chunk_frames", _i32), ("window_chunks", _i32), ("dtype", _i32),
         ("k", _vp), ("v", _vp), ("k_scale", _vp), ("v_scale", _vp),
         ("k_gscale", _vp), ("v_gscale", _vp), ("dev_ws", _vp),
+        ("attn_ws", _vp), ("attn_ws_bytes", ctypes.c_uint64),
         ("scrub_on_evict", _i32), ("init_magic", _i32),
         ("chunk_of_region", _i64 * (1 + KVC_MAX_WINDOW)),
         ("last_chunk", _i64),

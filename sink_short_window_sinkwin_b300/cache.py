@@ -35,7 +35,8 @@ class KVCache:
     """
 
     def __init__(self, heads: int, head_dim: int, tokens_per_frame: int, chunk_frames: int,
-                 window_chunks: int, dtype: str = "bf16", device="cuda", scrub_on_evict=False):
+                 window_chunks: int, dtype: str = "bf16", device="cuda", scrub_on_evict=False,
+                 attn_workspace: bool = True):
         self.c = KvcCache()
         c = self.c
         c.heads, c.head_dim = heads, head_dim
@@ -50,7 +51,7 @@ class KVCache:
         self.W = window_chunks
         self.S = (1 + window_chunks) * self.Tc
         L = lib()
-        nbytes = [L.kvc_cache_bytes(ctypes.byref(c), i) for i in range(7)]
+        nbytes = [L.kvc_cache_bytes(ctypes.byref(c), i) for i in range(8)]
         if nbytes[0] == 0:
             raise ValueError("invalid cache geometry")
         if dtype == "bf16":
@@ -66,6 +67,11 @@ class KVCache:
             self.k_gscale = torch.zeros(1 + window_chunks, dtype=torch.float32, device=self.device)
             self.v_gscale = torch.zeros_like(self.k_gscale)
         self.ws = torch.zeros(_abi.KVC_WS_WORDS, dtype=torch.int32, device=self.device)
+        # attention workspace: lets sinkwin_attn spread the work evenly over all SMs
+        self.attn_ws = (torch.zeros(nbytes[7], dtype=torch.uint8, device=self.device)
+                        if attn_workspace and nbytes[7] > 0 else None)
+        c.attn_ws = 0 if self.attn_ws is None else self.attn_ws.data_ptr()
+        c.attn_ws_bytes = 0 if self.attn_ws is None else nbytes[7]
         for name, t, nb in (("k", self.k, nbytes[0]), ("v", self.v, nbytes[1]),
                             ("k_scale", self.k_scale, nbytes[2]), ("v_scale", self.v_scale, nbytes[3]),
                             ("k_gscale", self.k_gscale, nbytes[4]), ("v_gscale", self.v_gscale, nbytes[5]),

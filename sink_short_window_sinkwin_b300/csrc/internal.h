@@ -58,8 +58,15 @@ struct AttnLaunch {
   const float* k_gscale;
   const float* v_gscale;
   int32_t chunk_tokens;  // rows per region (FP4: region of a row -> its tensor scale)
+  // split-item workspace (null: whole items per CTA)
+  void* ws;
+  size_t ws_bytes;
 };
 cudaError_t launch_sinkwin_attn(const AttnLaunch& a, cudaStream_t st);
+// bytes of the attention workspace for head dim D and `ctas` persistent CTAs
+size_t attn_workspace_bytes(int D, int ctas);
+// SMs of the current device (0 when there is none)
+int attn_sm_count();
 
 // ---- recache (kernels_recache.cu) ----
 struct RecacheLaunch {
@@ -78,6 +85,19 @@ struct RecacheLaunch {
 cudaError_t launch_recache(const RecacheLaunch& r, cudaStream_t st);
 // H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} and D even, D/2 <= 128
 bool recache_supported(int H, int D);
+
+// Raise a kernel's dynamic shared-memory limit once per device (the setting
+// is per function and device; repeating it on every launch costs host time).
+// `done` is a per-kernel flag array owned by the caller.
+template <typename K>
+cudaError_t set_smem_once(K kern, size_t bytes, bool (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
 
 // ---- diagnostics ----
 cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st);

@@ -6,19 +6,31 @@
 // Here: O = softmax(tau Q K^T) V per head over the visible cache rows, exact up
 // to floating-point rounding (bf16 operands, fp32 accumulation and softmax).
 //
-// One CTA = one head x two 128-row query tiles ("slots") that share every K/V
-// tile.  Warp roles (320 threads):
+// Work: an "item" is one head x two 128-row query tiles ("slots") that share
+// every K/V tile; a "step" is one item x one 128-key K/V tile.  The kernel is
+// persistent: G CTAs (at most one per SM) each take an equal contiguous share
+// of all items' steps, so the last wave is as full as the first.  An item cut
+// by a share boundary is computed in two pieces by neighbouring CTAs: CTA g+1
+// (whose share starts inside the item) writes its piece's unnormalised O and
+// (max, sum) rows to a workspace slot and raises a flag; CTA g (whose share
+// ends inside the item, and which reaches that piece last) waits for the flag
+// -- a bounded wait, in a cooperative launch -- and merges the two pieces.
+// Without a workspace the shares are whole items.
+//
+// Warp roles (320 threads; 448 with an FP4 cache):
 //   warps 0-3  softmax of slot 0 (thread i owns query row i: TMEM lane i)
 //   warps 4-7  softmax of slot 1
-//   warp  8    TMA producer: Q once, then K/V tiles of 128 keys, 2-stage ring
+//   warp  8    TMA producer: Q per piece, then K/V tiles through a 2-stage ring
 //   warp  9    TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 10-13 (FP4 cache only) dequantise K/V tiles into the smem ring
 // TMEM (512 columns): S0 [0,128) O0 [128,256) S1 [256,384) O1 [384,512);
-// P (bf16) overwrites the first 64 columns of S and feeds the P*V MMA from TMEM.
-// The running max is only moved when it grows by more than 2^8 (log2 domain),
-// so O is rescaled in TMEM rarely.
+// P (bf16; f16 for FP4) overwrites the first 64 columns of S and feeds the
+// P*V MMA from TMEM.  The running max only moves when it grows by more than
+// 2^8 (log2 domain), so O is rescaled in TMEM rarely.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -26,8 +38,8 @@
 namespace kvc {
 namespace {
 
-constexpr int BM = 128;        // query rows per slot
-constexpr int BN = 128;        // keys per K/V tile
+constexpr int BM = 128;  // query rows per slot
+constexpr int BN = 128;  // keys per K/V tile
 constexpr int kStages = 2;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kTmaWarp = 8;
@@ -36,12 +48,23 @@ constexpr int kDequantWarp0 = 10;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnParams {
-  int32_t tq, H, D, S, nt;  // nt: K/V tiles over all segments
+  int32_t tq, H, D, S, nt;  // nt: K/V tiles of one item (over all segments)
   int32_t nseg;
   Seg seg[kMaxSeg];
+  int32_t seg_t0[kMaxSeg];  // first tile of each segment
   float scale_log2;
   __nv_bfloat16* out;
   int32_t* dev_err;
+  // schedule
+  int32_t n_pairs;  // items per head
+  int32_t NI;       // items
+  int32_t G;        // CTAs
+  int32_t split;    // 1: step-balanced shares with merges; 0: whole items
+  int64_t NS;       // NI * nt
+  float* ws_o;      // [G][2*BM][D]     unnormalised O of a share's first piece
+  float2* ws_ml;    // [G][2*BM]        its (running max, running sum)
+  unsigned long long* ws_flag;  // [G]  == epoch once slot g is written
+  unsigned long long epoch;
   // FP4 cache
   const uint8_t* kc;
   const uint8_t* vc;
@@ -58,18 +81,24 @@ struct __align__(1024) AttnSmem {
   __nv_bfloat16 q[2][DB][BM * 64];
   __nv_bfloat16 k[kStages][DB][BN * 64];
   __nv_bfloat16 v[kStages][DB][BN * 64];
-  uint64_t bar_q;
+  uint64_t bar_q, bar_qempty;
   uint64_t bar_kfull[kStages], bar_kempty[kStages];
   uint64_t bar_vfull[kStages], bar_vempty[kStages];
-  uint64_t bar_s[2], bar_p[2];
+  uint64_t bar_s[2], bar_p[2], bar_o[2], bar_ofree[2];
+  uint64_t bar_part;  // all 256 partial rows of the share's first piece are written
   uint64_t bar_drain;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
-// Walk the visible segments tile by tile.
+// K/V tile cursor over the visible segments.
 struct KvCursor {
   int seg = 0, off = 0;
+  __device__ __forceinline__ void seek(const AttnParams& p, int t) {
+    seg = 0;
+    while (seg + 1 < p.nseg && p.seg_t0[seg + 1] <= t) ++seg;
+    off = (t - p.seg_t0[seg]) * BN;
+  }
   __device__ __forceinline__ int row0(const AttnParams& p) const { return p.seg[seg].row0 + off; }
   __device__ __forceinline__ int valid(const AttnParams& p) const {
     return min(BN, p.seg[seg].rows - off);
@@ -83,9 +112,30 @@ struct KvCursor {
   }
 };
 
+// A piece: item u, K/V tiles [t0, t1) of it.  Every role walks the same list.
+struct Piece {
+  int u, t0, t1;
+};
+struct Share {
+  int64_t s, e;
+  __device__ __forceinline__ bool next(const AttnParams& p, Piece& pc) {
+    if (s >= e) return false;
+    pc.u = (int)(s / p.nt);
+    pc.t0 = (int)(s - (int64_t)pc.u * p.nt);
+    pc.t1 = (int)min((int64_t)p.nt, pc.t0 + (e - s));
+    s += pc.t1 - pc.t0;
+    return true;
+  }
+};
+__device__ __forceinline__ Share share_of(const AttnParams& p, int g) {
+  if (p.split) return Share{(int64_t)g * p.NS / p.G, (int64_t)(g + 1) * p.NS / p.G};
+  const int64_t a = (int64_t)g * p.NI / p.G, b = (int64_t)(g + 1) * p.NI / p.G;
+  return Share{a * p.nt, b * p.nt};
+}
+
 // ---------------------------------------------------------------------------
-// FP4 tile dequantisation: thread i writes key row i of a K or V tile as bf16
-// in the 128-byte-swizzled layout the MMA descriptors expect.
+// FP4 tile dequantisation: thread i writes key row i of a K or V tile in the
+// 128-byte-swizzled layout the MMA descriptors expect.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t d;
@@ -164,6 +214,15 @@ __device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r
   }
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
 template <int D, bool kFp4>
 __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     sinkwin_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -176,14 +235,12 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int m0 = blockIdx.x * (2 * BM);
-  const bool active1 = (m0 + BM) < p.tq;
-  const int nt = p.nt;
+  const int g = blockIdx.x;
   const uint32_t kvfull_count = kFp4 ? 128u : 1u;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_q, 1);
+    mbar_init(&sm.bar_qempty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.bar_kfull[s], kvfull_count);
       mbar_init(&sm.bar_vfull[s], kvfull_count);
@@ -192,8 +249,11 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.bar_s[s], 1);
+      mbar_init(&sm.bar_o[s], 1);
       mbar_init(&sm.bar_p[s], BM);
+      mbar_init(&sm.bar_ofree[s], BM);
     }
+    mbar_init(&sm.bar_part, 2 * BM);
     mbar_init(&sm.bar_drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -218,62 +278,90 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t qbytes = (active1 ? 2u : 1u) * DB * BM * 64 * 2;
-      mbar_expect_tx(&sm.bar_q, qbytes);
-      for (int s = 0; s < (active1 ? 2 : 1); ++s)
-        for (int db = 0; db < DB; ++db)
-          tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
-      int issued = 0;
-      if (!kFp4) {
-        KvCursor cur;
-        const uint32_t tbytes = DB * BN * 64 * 2;
-        for (int t = 0; t < nt; ++t) {
-          const int st = t & 1, n = t >> 1;
-          if (t >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) break;
-          mbar_expect_tx(&sm.bar_kfull[st], tbytes);
+      Share sh = share_of(p, g);
+      Piece pc;
+      uint32_t it = 0;  // K/V tiles of this CTA so far (ring position)
+      int npc = 0, nk = 0, nv = 0;
+      bool ok = true;
+      while (ok && sh.next(p, pc)) {
+        const int h = pc.u / p.n_pairs;
+        const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+        const bool act1 = m0 + BM < p.tq;
+        if (npc > 0 && !mbar_wait(&sm.bar_qempty, (npc - 1) & 1, wd)) break;
+        mbar_expect_tx(&sm.bar_q, (act1 ? 2u : 1u) * DB * BM * 64 * 2);
+        for (int s = 0; s < (act1 ? 2 : 1); ++s)
           for (int db = 0; db < DB; ++db)
-            tma_load_3d(&sm.k[st][db][0], &tmK, &sm.bar_kfull[st], db * 64, h, cur.row0(p));
-          if (t >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
-            issued = -(t + 1);  // K of tile t issued, V not
-            break;
-          }
-          mbar_expect_tx(&sm.bar_vfull[st], tbytes);
-          for (int db = 0; db < DB; ++db)
-            tma_load_3d(&sm.v[st][db][0], &tmV, &sm.bar_vfull[st], db * 64, h, cur.row0(p));
-          cur.next(p);
-          issued = t + 1;
-        }
-        // teardown: every copy this thread started must land before the CTA exits
-        if (sm.abort_flag) {
-          const int nk = issued >= 0 ? issued : -issued;
-          const int nv = issued >= 0 ? issued : (-issued - 1);
-          for (int st = 0; st < kStages; ++st) {
-            const int ck = nk > st ? (nk - st + 1) / 2 : 0;  // uses of stage st
-            const int cv = nv > st ? (nv - st + 1) / 2 : 0;
-            if (ck) mbar_drain(&sm.bar_kfull[st], (ck - 1) & 1);
-            if (cv) mbar_drain(&sm.bar_vfull[st], (cv - 1) & 1);
+            tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
+        ++npc;
+        if (!kFp4) {
+          KvCursor cur;
+          cur.seek(p, pc.t0);
+          const uint32_t tbytes = DB * BN * 64 * 2;
+          for (int t = pc.t0; t < pc.t1; ++t, ++it) {
+            const int st = it & 1, n = it >> 1;
+            if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.bar_kfull[st], tbytes);
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(&sm.k[st][db][0], &tmK, &sm.bar_kfull[st], db * 64, h, cur.row0(p));
+            ++nk;
+            if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.bar_vfull[st], tbytes);
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(&sm.v[st][db][0], &tmV, &sm.bar_vfull[st], db * 64, h, cur.row0(p));
+            ++nv;
+            cur.next(p);
           }
         }
       }
-      mbar_drain(&sm.bar_q, 0);
+      // teardown after an abort: every copy this thread started must land
+      // before the CTA exits (the consumers waited for the rest)
+      if (sm.abort_flag) {
+        for (int st = 0; st < kStages; ++st) {
+          const int ck = nk > st ? (nk - st + 1) / 2 : 0;  // uses of stage st
+          const int cv = nv > st ? (nv - st + 1) / 2 : 0;
+          if (ck) mbar_drain(&sm.bar_kfull[st], (ck - 1) & 1);
+          if (cv) mbar_drain(&sm.bar_vfull[st], (cv - 1) & 1);
+        }
+        if (npc) mbar_drain(&sm.bar_q, (npc - 1) & 1);
+      }
     }
   } else if (kFp4 && warp >= kDequantWarp0) {
     // ------------------------------------------------------------ FP4 dequant producer
     const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
-    KvCursor cur;
-    for (int t = 0; t < nt; ++t) {
-      const int st = t & 1, n = t >> 1;
-      const int grow = cur.row0(p) + r;
-      const bool live = r < cur.valid(p);
-      if (t >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) break;
-      dequant_row<D, false>(sm.k[st], r, grow, live, p.kc, p.ks, p, h);
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.bar_kfull[st]);
-      if (t >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) break;
-      dequant_row<D, true>(sm.v[st], r, grow, live, p.vc, p.vs, p, h);
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.bar_vfull[st]);
-      cur.next(p);
+    Share sh = share_of(p, g);
+    Piece pc;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && sh.next(p, pc)) {
+      const int h = pc.u / p.n_pairs;
+      KvCursor cur;
+      cur.seek(p, pc.t0);
+      for (int t = pc.t0; t < pc.t1; ++t, ++it) {
+        const int st = it & 1, n = it >> 1;
+        const int grow = cur.row0(p) + r;
+        const bool live = r < cur.valid(p);
+        if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
+          ok = false;
+          break;
+        }
+        dequant_row<D, false>(sm.k[st], r, grow, live, p.kc, p.ks, p, h);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_kfull[st]);
+        if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
+          ok = false;
+          break;
+        }
+        dequant_row<D, true>(sm.v[st], r, grow, live, p.vc, p.vs, p, h);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_vfull[st]);
+        cur.next(p);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -301,44 +389,81 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           mma_bf16_ts(tO[slot], tS[slot] + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&sm.bar_q, 0, wd) && mbar_wait(&sm.bar_kfull[0], 0, wd);
-      if (ok) {
+      Share sh = share_of(p, g);
+      Piece pc;
+      uint32_t it = 0;
+      int npc = 0;
+      int np[2] = {0, 0}, nof[2] = {0, 0};
+      bool pend[2] = {false, false};  // an epilogue of this slot may still read O
+      bool ok = true;
+      while (ok && sh.next(p, pc)) {
+        const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+        const bool act1 = m0 + BM < p.tq;
+        const int n = pc.t1 - pc.t0;
+        const int st0 = it & 1;
+        ok = mbar_wait(&sm.bar_q, npc & 1, wd) && mbar_wait(&sm.bar_kfull[st0], (it >> 1) & 1, wd);
+        if (!ok) break;
         tc_fence_after();
-        qk(0, 0);
+        qk(0, st0);
         mma_commit(&sm.bar_s[0]);
-        if (active1) {
-          qk(1, 0);
+        if (act1) {
+          qk(1, st0);
           mma_commit(&sm.bar_s[1]);
         }
-        mma_commit(&sm.bar_kempty[0]);
-        for (int t = 0; t < nt && ok; ++t) {
-          const int st = t & 1, ph = (t >> 1) & 1;
-          const int nst = (t + 1) & 1, nph = ((t + 1) >> 1) & 1;
-          const bool more = t + 1 < nt;
-          ok = mbar_wait(&sm.bar_p[0], t & 1, wd) && mbar_wait(&sm.bar_vfull[st], ph, wd);
+        mma_commit(&sm.bar_kempty[st0]);
+        if (n == 1) mma_commit(&sm.bar_qempty);
+        for (int i = 0; i < n && ok; ++i) {
+          const uint32_t ti = it + i;
+          const int st = ti & 1, ph = (ti >> 1) & 1;
+          const int nst = (ti + 1) & 1, nph = ((ti + 1) >> 1) & 1;
+          const bool more = i + 1 < n;
+          ok = mbar_wait(&sm.bar_p[0], np[0] & 1, wd) && mbar_wait(&sm.bar_vfull[st], ph, wd);
+          ++np[0];
+          if (ok && i == 0 && pend[0]) {
+            ok = mbar_wait(&sm.bar_ofree[0], nof[0] & 1, wd);
+            ++nof[0];
+            pend[0] = false;
+          }
           if (!ok) break;
           tc_fence_after();
-          pv(0, st, t > 0);
+          pv(0, st, i > 0);
           if (more) {
             ok = mbar_wait(&sm.bar_kfull[nst], nph, wd);
             if (!ok) break;
             tc_fence_after();
             qk(0, nst);
+            mma_commit(&sm.bar_s[0]);
+          } else {
+            mma_commit(&sm.bar_o[0]);
           }
-          mma_commit(&sm.bar_s[0]);
-          if (active1) {
-            ok = mbar_wait(&sm.bar_p[1], t & 1, wd);
+          if (act1) {
+            ok = mbar_wait(&sm.bar_p[1], np[1] & 1, wd);
+            ++np[1];
+            if (ok && i == 0 && pend[1]) {
+              ok = mbar_wait(&sm.bar_ofree[1], nof[1] & 1, wd);
+              ++nof[1];
+              pend[1] = false;
+            }
             if (!ok) break;
             tc_fence_after();
-            pv(1, st, t > 0);
+            pv(1, st, i > 0);
             mma_commit(&sm.bar_vempty[st]);
-            if (more) qk(1, nst);
-            mma_commit(&sm.bar_s[1]);
+            if (more) {
+              qk(1, nst);
+              mma_commit(&sm.bar_s[1]);
+            } else {
+              mma_commit(&sm.bar_o[1]);
+            }
           } else {
             mma_commit(&sm.bar_vempty[st]);
           }
           if (more) mma_commit(&sm.bar_kempty[nst]);
+          if (i + 2 == n) mma_commit(&sm.bar_qempty);  // the piece's last QK went out above
         }
+        it += n;
+        ++npc;
+        pend[0] = true;
+        if (act1) pend[1] = true;
       }
       // drain: every MMA issued above completes before TMEM is released
       mma_commit(&sm.bar_drain);
@@ -349,52 +474,70 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     const int slot = warp >> 2;
     const int wq = warp & 3;
     const int row = threadIdx.x & (BM - 1);
-    if (slot == 0 || active1) {
-      const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-      const uint32_t tS = tmem + slot * 256 + lane_off;
-      const uint32_t tO = tS + 128;
-      const float c = p.scale_log2;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + slot * 256 + lane_off;
+    const uint32_t tO = tS + 128;
+    const float c = p.scale_log2;
+    Share sh = share_of(p, g);
+    Piece pc;
+    uint32_t it = 0;
+    int ns = 0, no = 0;
+    bool ok = true;
+    while (ok && sh.next(p, pc)) {
+      const int h = pc.u / p.n_pairs;
+      const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+      const bool act1 = m0 + BM < p.tq;
+      const int n = pc.t1 - pc.t0;
+      const uint32_t it0 = it;
+      it += n;
+      if (slot == 1 && !act1) continue;
       float m_ref = -INFINITY, l = 0.0f;
-      bool ok = true;
-      // keep a stale running max unless it grew by more than 2^8; then rescale
-      // O in TMEM (warp-collective ld/st, lanes that do not move keep factor 1)
-      auto rescale_if_needed = [&](int t, float mx_scaled, float& m_ref, float& l, uint32_t tO) {
+      // Keep a stale running max unless it grew by more than 2^8.  decide()
+      // moves the reference and returns the factor for O (1 when unchanged);
+      // apply() rescales O in TMEM, warp-collectively, once P is written (the
+      // P*V MMA of this tile only starts after this warp's P arrival), so the
+      // S row and the O chunk are never live in registers together.
+      auto decide = [&](int i, float mx_scaled) -> float {
         const float m_new = fmaxf(m_ref, mx_scaled);
-        if (t == 0) {
+        if (i == 0) {
           m_ref = m_new;
-          return;
+          return 1.0f;
         }
         const bool need = m_new > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;
-          if (need) m_ref = m_new;
-          l *= alpha;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;
+        if (need) m_ref = m_new;
+        l *= alpha;
+        return alpha;
+      };
+      auto apply = [&](float alpha) {
+        if (!__any_sync(0xffffffffu, alpha != 1.0f)) return;
+#pragma unroll 1
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tO + j * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t o[32];
-            tmem_ld32(tO + j * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + j * 32, o);
-          }
-          tmem_st_wait();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + j * 32, o);
         }
       };
       KvCursor cur;
-      for (int t = 0; t < nt; ++t) {
+      cur.seek(p, pc.t0);
+      for (int i = 0; i < n; ++i) {
         // warp-uniform exit: the tcgen05.ld/st below are warp-collective
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], t & 1, wd))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], ns & 1, wd))) {
           ok = false;
           break;
         }
+        ++ns;
         tc_fence_after();
         const int valid = cur.valid(p);
         if (!kFp4 && slot == 0 && valid < BN) {
           // key rows past the segment end may hold anything (NaN scrub,
           // never-written memory): zero them in the V stage before P*V
-          const int st = t & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_vfull[st], (t >> 1) & 1, wd))) {
+          const uint32_t ti = it0 + i;
+          const int st = ti & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_vfull[st], (ti >> 1) & 1, wd))) {
             ok = false;
             break;
           }
@@ -414,28 +557,43 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           for (int j = 0; j < BN / 32; ++j)
             tmem_ld32(tS + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[j * 32]));
           tmem_ld_wait();
-          float mx = -INFINITY;
+          if (valid < BN) {  // ragged tile (warp-uniform): keys past the end do not count
 #pragma unroll
-          for (int j = 0; j < BN; ++j) {
-            if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(sr[j]));
+            for (int j = 0; j < BN; ++j)
+              if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
           }
-          rescale_if_needed(t, mx * c, m_ref, l, tO);
-          const float neg = -m_ref;
-          float sum = 0.0f;
+          // row max: four independent 3-input max chains
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int j = 0; j < BN; j += 8)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              m4[q] = fmax3(m4[q], __uint_as_float(sr[j + 2 * q]), __uint_as_float(sr[j + 2 * q + 1]));
+          const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+          const float alpha = decide(i, mx * c);
+          // p = 2^(s*c - m): one packed FFMA per pair, packed row sum, bf16 pairs
+          // written back over the consumed S columns
+          const uint64_t c2 = f32x2(c, c), n2 = f32x2(-m_ref, -m_ref);
+          uint64_t acc2 = f32x2(0.0f, 0.0f);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j * 64 + 2 * e]), c, neg));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j * 64 + 2 * e + 1]), c, neg));
-              sum += p0 + p1;
+              const uint64_t y2 = ffma2(f32x2(__uint_as_float(sr[j * 64 + 2 * e]),
+                                              __uint_as_float(sr[j * 64 + 2 * e + 1])), c2, n2);
+              float y0, y1;
+              f32x2_split(y2, y0, y1);
+              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+              acc2 = fadd2(acc2, f32x2(p0, p1));
               pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st32(tS + j * 32, pk);
           }
-          l += sum;
+          float s0, s1;
+          f32x2_split(acc2, s0, s1);
+          l += s0 + s1;
+          apply(alpha);
         } else {
           // two passes over 32-column chunks (fewer live registers).  The tile
           // lies in one region: its K tensor scale joins the logit scale, its
@@ -450,10 +608,11 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
             tmem_ld32(tS + j * 32, sr);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (j * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(sr[e]));
+            for (int e = 0; e < 32; e += 2)
+              mx = fmax3(mx, j * 32 + e < valid ? __uint_as_float(sr[e]) : -INFINITY,
+                         j * 32 + e + 1 < valid ? __uint_as_float(sr[e + 1]) : -INFINITY);
           }
-          rescale_if_needed(t, mx * cg, m_ref, l, tO);
+          const float alpha = decide(i, mx * cg);
           const float neg = -m_ref;
           float sum = 0.0f;
 #pragma unroll
@@ -476,35 +635,118 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
             tmem_st16(tS + j * 16, pk);
           }
           l += sum;
+          apply(alpha);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.bar_p[slot]);
         cur.next(p);
       }
-      if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], nt & 1, wd))) {
-        tc_fence_after();
-        const int grow = m0 + slot * BM + row;
-        const float inv_l = 1.0f / l;
-        __nv_bfloat16* dst = p.out + ((size_t)grow * p.H + h) * D;
+      if (!ok) break;
+      // ---- epilogue of the piece: O of its final tile is complete
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_o[slot], no & 1, wd))) {
+        ok = false;
+        break;
+      }
+      ++no;
+      tc_fence_after();
+      const int prow = slot * BM + row;  // row within the item's 256
+      const int grow = m0 + prow;
+      const bool head = pc.t0 == 0, tail = pc.t1 == p.nt;
+      const float* wsb = nullptr;  // partner piece to merge (head && !tail)
+      float mo = 0.0f, lo = 0.0f;
+      if (head && !tail) {
+        // the share's last piece, starting this item: merge with CTA g+1's
+        const unsigned long long* f = p.ws_flag + g + 1;
+        const uint64_t t0 = globaltimer_ns();
+        bool got = true;
+        while (ld_acquire_gpu_u64(f) != p.epoch) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            sm.abort_flag = 1;
+            if (p.dev_err) atomicCAS(p.dev_err, DEVERR_NONE, DEVERR_TIMEOUT);
+            got = false;
+            break;
+          }
+        }
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        wsb = p.ws_o + ((size_t)(g + 1) * 2 * BM + prow) * D;
+        const float2 ml = p.ws_ml[(size_t)(g + 1) * 2 * BM + prow];
+        mo = ml.x;
+        lo = ml.y;
+      }
+      float fa = 1.0f, fb = 0.0f, inv_l = 0.0f;
+      if (head && !tail) {
+        const float mm = fmaxf(m_ref, mo);
+        fa = ex2_approx(m_ref - mm);
+        fb = ex2_approx(mo - mm);
+        inv_l = 1.0f / (l * fa + lo * fb);
+      } else if (head) {
+        inv_l = 1.0f / l;
+      }
+      float* wsw = nullptr;  // this piece handed to CTA g-1 (!head)
+      if (!head) {
+        wsw = p.ws_o + ((size_t)g * 2 * BM + prow) * D;
+        p.ws_ml[(size_t)g * 2 * BM + prow] = make_float2(m_ref, l);
+      }
+      __nv_bfloat16* dst = p.out + ((size_t)grow * p.H + h) * D;
+#pragma unroll 1
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t o[32];
+        tmem_ld32(tO + j * 32, o);
+        tmem_ld_wait();
+        if (!head) {  // partial: unnormalised fp32 for the merging CTA
+          float4* w4 = reinterpret_cast<float4*>(wsw + j * 32);
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-          uint32_t o[32];
-          tmem_ld32(tO + j * 32, o);
-          tmem_ld_wait();
-          if (grow < p.tq) {
+          for (int e = 0; e < 8; ++e)
+            w4[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+          continue;
+        }
+        float x[32];
+        if (!tail) {
+          const float4* r4 = reinterpret_cast<const float4*>(wsb + j * 32);
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(dst + j * 32 + e) = w;
-            }
+          for (int e = 0; e < 8; ++e) {
+            const float4 b = r4[e];
+            x[4 * e + 0] = (__uint_as_float(o[4 * e + 0]) * fa + b.x * fb) * inv_l;
+            x[4 * e + 1] = (__uint_as_float(o[4 * e + 1]) * fa + b.y * fb) * inv_l;
+            x[4 * e + 2] = (__uint_as_float(o[4 * e + 2]) * fa + b.z * fb) * inv_l;
+            x[4 * e + 3] = (__uint_as_float(o[4 * e + 3]) * fa + b.w * fb) * inv_l;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]) * inv_l;
+        }
+        if (grow < p.tq) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(x[e + 0], x[e + 1]);
+            w.y = pack_bf16x2(x[e + 2], x[e + 3]);
+            w.z = pack_bf16x2(x[e + 4], x[e + 5]);
+            w.w = pack_bf16x2(x[e + 6], x[e + 7]);
+            *reinterpret_cast<uint4*>(dst + j * 32 + e) = w;
           }
         }
       }
+      if (!head) {
+        // publish slot g once every row of both slots is written (a share's
+        // first piece is the only one that can end an item it did not start,
+        // so bar_part completes at most once per launch: parity 0)
+        mbar_arrive(&sm.bar_part);
+        if (threadIdx.x == 0) {
+          if (!act1) mbar_arrive_count(&sm.bar_part, BM);  // slot 1 has no rows here
+          if (mbar_wait(&sm.bar_part, 0, wd)) {
+            __threadfence();
+            st_release_gpu_u64(p.ws_flag + g, p.epoch);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.bar_ofree[slot]);
     }
   }
 
@@ -515,6 +757,18 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+int sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
 }
 
 template <int D, bool kFp4>
@@ -541,6 +795,7 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   int nt = 0;
   for (int i = 0; i < a.nseg; ++i) {
     p.seg[i] = a.seg[i];
+    p.seg_t0[i] = nt;
     nt += (a.seg[i].rows + BN - 1) / BN;
   }
   p.nt = nt;
@@ -554,19 +809,53 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   p.kg = a.k_gscale;
   p.vg = a.v_gscale;
   p.Tc = a.chunk_tokens;
+  // schedule: at most one CTA per SM and per item, so every item spans at
+  // most two neighbouring shares
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  p.n_pairs = (a.tq + 2 * BM - 1) / (2 * BM);
+  p.NI = p.n_pairs * a.H;
+  p.NS = (int64_t)p.NI * nt;
+  p.G = p.NI < nsm ? p.NI : nsm;
+  const size_t need = attn_workspace_bytes(a.D, p.G);
+  p.split = (a.ws != nullptr && a.ws_bytes >= need && p.G > 1 && p.NI % p.G != 0) ? 1 : 0;
+  if (p.split) {
+    uint8_t* w = static_cast<uint8_t*>(a.ws);
+    p.ws_o = reinterpret_cast<float*>(w);
+    p.ws_ml = reinterpret_cast<float2*>(w + (size_t)p.G * 2 * BM * a.D * 4);
+    p.ws_flag = reinterpret_cast<unsigned long long*>(w + (size_t)p.G * 2 * BM * (a.D * 4 + 8));
+    static std::atomic<unsigned long long> epochs{0};
+    p.epoch = epochs.fetch_add(1) + 1;
+  }
   // one CTA per SM: a second resident CTA would wait in tcgen05.alloc for the
   // 512 TMEM columns the first one holds
   size_t smem = sizeof(AttnSmem<D>) + 1024;
   if (smem < 120 * 1024) smem = 120 * 1024;
   auto kern = sinkwin_attn_kernel<D, kFp4>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool smem_set[64] = {};  // one per instantiation of this launcher
+  cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.tq + 2 * BM - 1) / (2 * BM), a.H);
-  kern<<<grid, kFp4 ? 448 : 320, smem, st>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.G, 1, 1);
+  cfg.blockDim = dim3(kFp4 ? 448 : 320, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  // a merge waits on a neighbouring CTA: all CTAs must be resident together
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.split ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace
+
+size_t attn_workspace_bytes(int D, int ctas) {
+  return (size_t)ctas * 2 * BM * ((size_t)D * 4 + 8) + (size_t)ctas * 8;
+}
+
+int attn_sm_count() { return sm_count(); }
 
 cudaError_t launch_sinkwin_attn(const AttnLaunch& a, cudaStream_t st) {
   if (a.D == 128) return a.fp4 ? launch_attn_t<128, true>(a, st) : launch_attn_t<128, false>(a, st);

@@ -261,7 +261,8 @@ cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, 
                         cudaStream_t st) {
   const size_t smem = sizeof(GemmSmem<BN>) + 1024;
   auto kern = recache_gemm_kernel<BN, kKf32>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool smem_set[64] = {};  // one per instantiation of this launcher
+  cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.HD / BN, (rows + RM - 1) / RM);
   kern<<<grid, kRThreads, smem, st>>>(ta, tb, p);

@@ -178,6 +178,10 @@ size_t kvc_cache_bytes(const kvc_cache* c, int32_t which) {
       return c->dtype == KVC_FP4 ? (size_t)(1 + c->window_chunks) * sizeof(float) : 0;
     case 6:
       return (size_t)KVC_WS_WORDS * sizeof(int32_t);
+    case 7: {
+      const int nsm = attn_sm_count();
+      return nsm > 0 ? attn_workspace_bytes(c->head_dim, nsm) : 0;
+    }
     default:
       return 0;
   }
@@ -187,6 +191,7 @@ int32_t kvc_init(kvc_cache* c) {
   if (!geometry_ok(c)) return KVC_EINVAL;
   if (!c->k || !c->v || !c->dev_ws || !aligned16(c->k) || !aligned16(c->v) || !aligned16(c->dev_ws))
     return KVC_EINVAL;
+  if (c->attn_ws && !aligned16(c->attn_ws)) return KVC_EINVAL;
   if (c->dtype == KVC_FP4) {
     if (!c->k_scale || !c->v_scale || !c->k_gscale || !c->v_gscale) return KVC_EINVAL;
     if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVC_EINVAL;
@@ -301,6 +306,8 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, f
   a.k_gscale = c->k_gscale;
   a.v_gscale = c->v_gscale;
   a.chunk_tokens = Tc;
+  a.ws = c->attn_ws;
+  a.ws_bytes = c->attn_ws ? (size_t)c->attn_ws_bytes : 0;
   return cuda_status(launch_sinkwin_attn(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -110,6 +110,33 @@ def test_small_shapes_full_compare(swl, H, D, tpf, cf, W, tq):
         assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"{(H, D, tpf, cf, W, tq)} step {c}")
 
 
+@pytest.mark.parametrize("workspace", [True, False])
+def test_many_items_full_compare(swl, workspace):
+    """12 heads x 4680 queries = 228 items on at most 148 CTAs: with the
+    workspace, shares are step-balanced and most items are computed in two
+    pieces by neighbouring CTAs and merged; without it each CTA takes whole
+    items.  Short 100-token chunks keep the full oracle compare cheap."""
+    sh = Shapes(12, 128, 100, 1, 2, 10, 10)
+    scale = 1.0 / math.sqrt(128)
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, attn_workspace=workspace)
+    model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    for c in range(4):
+        _, k, v = chunk_qkv(sh, 12, 0, c, "rms1")
+        if c > sh.window_chunks:
+            cache.evict(c - sh.window_chunks)
+            model.evict(c - sh.window_chunks)
+        cache.append(k.cuda(), v.cuda(), c)
+        model.append(c, bf16_to_f64(k), bf16_to_f64(v))
+        if c in (0, 3):  # one segment of 1 tile; then two segments (hole-free ring wrap)
+            qq = chunk_qkv(sh, 13, 0, c, "rms1", q_rows=4680)[0]
+            out = cache.attn(qq.cuda(), scale)
+            torch.cuda.synchronize()
+            want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
+            assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"228 items, step {c}")
+    assert cache.last_device_error() == swl.KVC_OK
+
+
 def test_holes_scrub_and_zero_queries(swl):
     """Evict without append leaves a hole (two KV segments); the scrubbed slot
     holds NaN and must never reach the output."""

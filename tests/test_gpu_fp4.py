@@ -101,7 +101,8 @@ def test_fp4_tiny_stream(swl):
         out = cache.attn(q.cuda(), scale)
         torch.cuda.synchronize()
         want = oatt.sinkwin_attention(model, bf16_to_f64(q), scale)
-        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 tiny step {c}")
+        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 tiny step {c}",
+                 plus_output_rounding=True)
 
 
 @pytest.mark.parametrize("H,D,tpf,cf,W,tq", [(2, 128, 100, 1, 3, 130), (3, 64, 50, 3, 2, 300)])
@@ -113,7 +114,8 @@ def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
         out = cache.attn(qq.cuda(), scale)
         torch.cuda.synchronize()
         want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
-        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 {(H, D, tpf, cf, W, tq)} step {c}")
+        assert_close(to64(out), want, ATOL_FP4, None, f"fp4 {(H, D, tpf, cf, W, tq)} step {c}",
+                 plus_output_rounding=True)
 
 
 def test_fp4_layer_full_size(swl):
@@ -124,5 +126,22 @@ def test_fp4_layer_full_size(swl):
     torch.cuda.synchronize()
     kk, vv = model.visible_kv()
     want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, SAMPLE_ROWS_4680)
-    print(assert_close(to64(out)[SAMPLE_ROWS_4680], want, ATOL_FP4, None, "fp4 layer"))
+    print(assert_close(to64(out)[SAMPLE_ROWS_4680], want, ATOL_FP4, None, "fp4 layer",
+                 plus_output_rounding=True))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_fp4_many_items_full_compare(swl):
+    """FP4 cache, 228 items on 148 CTAs (step-balanced shares, merged pieces),
+    one segment per region, full compare of all 4680 x 12 rows."""
+    sh = Shapes(12, 128, 100, 1, 2, 10, 10)
+    scale = 1.0 / math.sqrt(128)
+    for c, q, cache, model in _fp4_stream(swl, sh, 14, 4, "outliers"):
+        if c in (0, 3):
+            qq = chunk_qkv(sh, 15, 0, c, "rms1", q_rows=4680)[0]
+            out = cache.attn(qq.cuda(), scale)
+            torch.cuda.synchronize()
+            want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
+            assert_close(to64(out), want, ATOL_FP4, None, f"fp4 228 items step {c}",
+                 plus_output_rounding=True)
     assert cache.last_device_error() == swl.KVC_OK
