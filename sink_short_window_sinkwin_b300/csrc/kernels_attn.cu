@@ -103,34 +103,51 @@ struct KvCursor {
   __device__ __forceinline__ int valid(const AttnParams& p) const {
     return min(BN, p.seg[seg].rows - off);
   }
-  __device__ __forceinline__ void next(const AttnParams& p) {
+  __device__ __forceinline__ void next(const AttnParams& p) {  // wraps after the last tile
     off += BN;
     if (off >= p.seg[seg].rows) {
-      ++seg;
       off = 0;
+      if (++seg >= p.nseg) seg = 0;
     }
   }
 };
 
-// A piece: item u, K/V tiles [t0, t1) of it.  Every role walks the same list.
+// A piece: item u, logical K/V tiles [t0, t1) of it.  Every role walks the same list.
+// Softmax does not see key order, so a piece may visit its item's K/V tiles in
+// any order.  Tiles are visited rotated so that at local step tau of every
+// share the tile is about tau mod nt: CTAs working on the same head then read
+// the same tile at about the same time and share it through L2.  Both pieces
+// of a split item take the rotation of the piece that ends it (its share
+// starts with it), so together they still visit every tile once.
 struct Piece {
   int u, t0, t1;
+  int rot;  // physical tile of logical tile t is (t + rot) mod nt
 };
 struct Share {
-  int64_t s, e;
+  int64_t b, s, e;
   __device__ __forceinline__ bool next(const AttnParams& p, Piece& pc) {
     if (s >= e) return false;
     pc.u = (int)(s / p.nt);
     pc.t0 = (int)(s - (int64_t)pc.u * p.nt);
     pc.t1 = (int)min((int64_t)p.nt, pc.t0 + (e - s));
+    if (pc.t0 > 0) pc.rot = (p.nt - pc.t0) % p.nt;        // ends an item started elsewhere
+    else if (pc.t1 < p.nt) pc.rot = (p.nt - pc.t1) % p.nt;  // starts an item finished elsewhere
+    else pc.rot = (int)((s - b) % p.nt);                    // a whole item
     s += pc.t1 - pc.t0;
     return true;
   }
+  // first physical tile of the piece
+  __device__ __forceinline__ static int first_tile(const AttnParams& p, const Piece& pc) {
+    return (pc.t0 + pc.rot) % p.nt;
+  }
 };
 __device__ __forceinline__ Share share_of(const AttnParams& p, int g) {
-  if (p.split) return Share{(int64_t)g * p.NS / p.G, (int64_t)(g + 1) * p.NS / p.G};
-  const int64_t a = (int64_t)g * p.NI / p.G, b = (int64_t)(g + 1) * p.NI / p.G;
-  return Share{a * p.nt, b * p.nt};
+  if (p.split) {
+    const int64_t b = (int64_t)g * p.NS / p.G;
+    return Share{b, b, (int64_t)(g + 1) * p.NS / p.G};
+  }
+  const int64_t a = (int64_t)g * p.NI / p.G, z = (int64_t)(g + 1) * p.NI / p.G;
+  return Share{a * p.nt, a * p.nt, z * p.nt};
 }
 
 // ---------------------------------------------------------------------------
@@ -295,7 +312,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
         ++npc;
         if (!kFp4) {
           KvCursor cur;
-          cur.seek(p, pc.t0);
+          cur.seek(p, Share::first_tile(p, pc));
           const uint32_t tbytes = DB * BN * 64 * 2;
           for (int t = pc.t0; t < pc.t1; ++t, ++it) {
             const int st = it & 1, n = it >> 1;
@@ -341,7 +358,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     while (ok && sh.next(p, pc)) {
       const int h = pc.u / p.n_pairs;
       KvCursor cur;
-      cur.seek(p, pc.t0);
+      cur.seek(p, Share::first_tile(p, pc));
       for (int t = pc.t0; t < pc.t1; ++t, ++it) {
         const int st = it & 1, n = it >> 1;
         const int grow = cur.row0(p) + r;
@@ -522,7 +539,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
         }
       };
       KvCursor cur;
-      cur.seek(p, pc.t0);
+      cur.seek(p, Share::first_tile(p, pc));
       for (int i = 0; i < n; ++i) {
         // warp-uniform exit: the tcgen05.ld/st below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_s[slot], ns & 1, wd))) {

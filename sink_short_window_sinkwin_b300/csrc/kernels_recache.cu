@@ -232,25 +232,35 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
   // the K row is overwritten in place: every lane's reads of it come first
   __syncwarp();
   uint2* out = reinterpret_cast<uint2*>(p.k + dest * HD);
+  // the two rotation pairs of a float4; when D divides 128 they are the same
+  // pairs in every head, so their angles are evaluated once per row
+  int pr_cached = -1;
+  float cs[2] = {1.0f, 1.0f}, sn[2] = {0.0f, 0.0f};
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int c4 = lane + 32 * i;
     if (c4 >= HD / 4) break;
     const int col = 4 * c4;
+    const int pr0 = (col % p.D) >> 1;  // pairs pr0, pr0 + 1 (col is a multiple of 4)
+    if (pr0 != pr_cached) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int pr = pr0 + e;
+        const float pos = pr < p.pf ? pos_f : (pr < p.pf + p.ph ? pos_h : pos_w);
+        sincosf(pos * p.omega[pr], &sn[e], &cs[e]);
+      }
+      pr_cached = pr0;
+    }
     const float v4[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
     uint32_t o[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int c = col + 2 * e;
-      const int pr = (c % p.D) >> 1;
       const float g0 = p.gamma ? p.gamma[c] : 1.0f;
       const float g1 = p.gamma ? p.gamma[c + 1] : 1.0f;
       const float y0 = v4[2 * e] * rstd * g0;
       const float y1 = v4[2 * e + 1] * rstd * g1;
-      const float pos = pr < p.pf ? pos_f : (pr < p.pf + p.ph ? pos_h : pos_w);
-      float sn, cs;
-      sincosf(pos * p.omega[pr], &sn, &cs);
-      o[e] = pack_bf16x2(y0 * cs - y1 * sn, y0 * sn + y1 * cs);
+      o[e] = pack_bf16x2(y0 * cs[e] - y1 * sn[e], y0 * sn[e] + y1 * cs[e]);
     }
     out[c4] = make_uint2(o[0], o[1]);
   }
