@@ -207,6 +207,60 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# HBM-bound kernels, timed back to back
+# ---------------------------------------------------------------------------
+def hbm_kernels(swl, dev, layers, randn, reps: int = 16):
+    """Per-launch time of the bandwidth kernels with CUDA events around `reps`
+    back-to-back launches (no host gap inside), sources rotating over the layer
+    inputs (> L2 in total): bf16 append (copy), FP4 append (amax + encode) and
+    the NaN scrub of a slot on evict."""
+    import torch
+    srcs = [(L["k"], L["v"]) for L in layers]
+    srcs4 = [(L["k4"], L["v4"]) for L in layers]
+    while len(srcs) < 8:  # keep the rotating sources larger than L2
+        srcs.append((randn((TC, H, D)), randn((TC, H, D))))
+        srcs4.append((randn((TC, H, D), outliers=True), randn((TC, H, D), outliers=True)))
+    out = {}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    for name, dt, src, nbytes in (("append_bf16", "bf16", srcs, APPEND_BF16_BYTES),
+                                  ("append_fp4", "fp4", srcs4, APPEND_FP4_BYTES)):
+        cache = swl.KVCache(H, D, TPF, CF, W, dtype=dt, device=dev)
+        for c in range(1 + W):
+            cache.append(*src[c % len(src)], c)
+        for i in range(3):  # warm-up: re-append the newest chunk (overwrite)
+            cache.append(*src[i % len(src)], W)
+        a, b = ev(), ev()
+        torch.cuda.synchronize()
+        a.record()
+        for i in range(reps):
+            cache.append(*src[i % len(src)], W)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out[name] = {"us": ms * 1e3, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+
+    for name, dt, nbytes in (("evict_scrub_bf16", "bf16", 2 * TC * HD * 2),
+                             ("evict_scrub_fp4", "fp4", 2 * (TC * HD // 2 + TC * HD // 16))):
+        cache = swl.KVCache(H, D, TPF, CF, W, dtype=dt, device=dev, scrub_on_evict=True)
+        src = srcs if dt == "bf16" else srcs4
+        for c in range(1 + W):
+            cache.append(*src[c % len(src)], c)
+        evs = [(ev(), ev()) for _ in range(reps + 3)]
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            c = 1 + W + i
+            a.record()
+            cache.evict(c - W)  # one fill launch over the freed slot
+            b.record()
+            cache.append(*src[c % len(src)], c)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs[3:]) / reps
+        out[name] = {"us": ms * 1e3, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    return out
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def main():
@@ -359,6 +413,8 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = STEP_FLOP * world / (e2e_ms * 1e-3) / 1e12
 
+    hbm = hbm_kernels(swl, dev, layers, randn)
+
     for L in layers:
         for cache in (L["bf"], L["f4"]):
             st = cache.last_device_error()
@@ -370,7 +426,9 @@ def main():
             dist.destroy_process_group()
         return
 
-    peak, peak_sus, hbm, peak_src = _peaks()
+    peak, peak_sus, hbm_peak, peak_src = _peaks()
+    for r in hbm.values():
+        r["frac_hbm_peak"] = r["gbs"] / hbm_peak
     steps = args.steps
     per = {r: row_ms[r] / steps for r in ROWS}
     flops = {"recache": RECACHE_FLOP, "attn_bf16": ATTN_FLOP, "attn_fp4": ATTN_FLOP}
@@ -385,7 +443,7 @@ def main():
         if r in bytes_ and per[r] > 0:
             d["gbs"] = bytes_[r] / (per[r] * 1e-3) / 1e9
             if r.startswith("append"):
-                d["frac_hbm_peak"] = d["gbs"] / hbm
+                d["frac_hbm_peak"] = d["gbs"] / hbm_peak
         if r.startswith("attn") and per[r] > 0:
             d["latent_frames_per_s_per_layer"] = CF / (per[r] * 1e-3)
         rows[r] = d
@@ -416,6 +474,7 @@ def main():
                      "traffic": traffic},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "hbm_kernels": hbm,
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,

@@ -99,7 +99,8 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
 __global__ void __launch_bounds__(kMemThreads) amax_kernel(QuantJobs jobs, int64_t n,
                                                            int32_t* __restrict__ ws) {
   __shared__ uint32_t red[32];
-  const uint4* x = reinterpret_cast<const uint4*>(jobs.j[blockIdx.y].x);
+  // select, not index: a dynamic index would copy the parameter struct to local memory
+  const uint4* x = reinterpret_cast<const uint4*>(blockIdx.y ? jobs.j[1].x : jobs.j[0].x);
   const int64_t n8 = n >> 3;
   uint32_t acc2 = 0;
   const int64_t stride = (int64_t)gridDim.x * kMemThreads;
@@ -118,21 +119,12 @@ __global__ void __launch_bounds__(kMemThreads) amax_kernel(QuantJobs jobs, int64
   if (threadIdx.x == 0) ws[blockIdx.y * kQuantPartials + blockIdx.x] = (int32_t)m;
 }
 
-// E4M3 (bias 7, 3 mantissa bits, subnormal quantum 2^-9, max 448) of x >= 0:
-// round to nearest, ties to even, saturating at 448.
+// E4M3 code of x >= 0, round to nearest even, saturating at 448 (the
+// hardware conversion; OCP E4M3: bias 7, subnormal quantum 2^-9)
 __device__ __forceinline__ uint32_t e4m3_rne_satfinite(float x) {
-  if (x >= 448.0f) return 0x7Eu;
-  if (x < 0.015625f) {                      // below 2^-6: multiples of 2^-9
-    return (uint32_t)__float2int_rn(x * 512.0f);  // exact scaling, RNE to integer (8 -> 0x08)
-  }
-  const uint32_t b = __float_as_uint(x);
-  const int e = (int)(b >> 23) - 127;       // -6 .. 8
-  const uint32_t mant = b & 0x7FFFFFu;
-  uint32_t m = mant >> 20;
-  const uint32_t rem = mant & 0xFFFFFu;
-  if (rem > 0x80000u || (rem == 0x80000u && (m & 1u))) ++m;
-  const uint32_t code = ((uint32_t)(e + 7) << 3) + m;  // m == 8 carries into the exponent
-  return code > 0x7Eu ? 0x7Eu : code;
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(e) : "f"(0.0f), "f"(x));
+  return (uint32_t)e & 0xFFu;  // the second operand lands in the low byte
 }
 
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
@@ -141,12 +133,14 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
 }
 
-// E2M1 magnitude code of t >= 0: the grid {0,.5,1,1.5,2,3,4,6}; a value on a
-// midpoint goes to the even code, anything above 6 to code 7.
-__device__ __forceinline__ uint32_t e2m1_rne_satfinite(float t) {
-  return (uint32_t)(t > 0.25f) + (uint32_t)(t >= 0.75f) + (uint32_t)(t > 1.25f) +
-         (uint32_t)(t >= 1.75f) + (uint32_t)(t > 2.5f) + (uint32_t)(t >= 3.5f) +
-         (uint32_t)(t > 5.0f);
+// Two E2M1 codes (sign | magnitude, round to nearest even, saturating at 6):
+// lo in the low nibble.  The sign of a value that rounds to 0 is kept.
+__device__ __forceinline__ uint32_t e2m1x2_rne_satfinite(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -157,7 +151,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __global__ void __launch_bounds__(kMemThreads) quant_kernel(QuantJobs jobs, int64_t n,
                                                             const int32_t* __restrict__ ws) {
   __shared__ uint32_t red[32];
-  const QuantJob job = jobs.j[blockIdx.y];
+  const QuantJob job = blockIdx.y ? jobs.j[1] : jobs.j[0];
   uint32_t m = 0;
   for (int i = threadIdx.x; i < kQuantPartials; i += kMemThreads)
     m = max(m, (uint32_t)ws[blockIdx.y * kQuantPartials + i]);
@@ -183,12 +177,11 @@ __global__ void __launch_bounds__(kMemThreads) quant_kernel(QuantJobs jobs, int6
       const float sg = __fmul_rn(e4m3_value(s), g);
       if (s != 0 && sg != 0.0f) {
         const float inv = __frcp_rn(sg);
+        // |x| * inv and x * inv round to the same magnitude; the sign rides along
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float a = bf16_lo(w[k]), bb = bf16_hi(w[k]);
-          const uint32_t c0 = ((w[k] >> 12) & 0x8u) | e2m1_rne_satfinite(__fmul_rn(fabsf(a), inv));
-          const uint32_t c1 = ((w[k] >> 28) & 0x8u) | e2m1_rne_satfinite(__fmul_rn(fabsf(bb), inv));
-          const uint32_t byte = c0 | (c1 << 4);
+          const uint32_t byte =
+              e2m1x2_rne_satfinite(__fmul_rn(bf16_lo(w[k]), inv), __fmul_rn(bf16_hi(w[k]), inv));
           if (k < 4) lo |= byte << (8 * k);
           else hi |= byte << (8 * (k - 4));
         }
