@@ -49,7 +49,12 @@ WORKLOAD = ("LongLive-1.3B layer chunk step: 12 heads x 128, 4680 queries/chunk,
             "recache 18720x1536x3072")
 # ncu dram bytes per launch of the dominant kernel, with the hash of the source
 # they were taken on (null once the kernel changed)
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --set full on the LongLive-1.3B layer workload (one launch each);
+    # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
+    "sinkwin_attn_kernel<128,false>": {"bytes": 311548160 + 25610496, "src_sha": "c125c3524c407684"},
+    "sinkwin_attn_kernel<128,true>": {"bytes": 49463040 + 6691072, "src_sha": "c125c3524c407684"},
+}
 
 
 def _peaks():
