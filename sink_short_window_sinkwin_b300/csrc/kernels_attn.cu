@@ -167,14 +167,37 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
+// One key row of FP4 codes and block scales, held in registers so the loads
+// for the next tile can be in flight while this one is decoded.
+template <int D>
+struct RawRow {
+  uint4 c[D / 32];      // 16 code bytes = 32 elements each
+  uint32_t s[D / 64];   // 4 E4M3 scale bytes each
+};
+template <int D>
+__device__ __forceinline__ void load_raw(RawRow<D>& raw, const uint8_t* codes, const uint8_t* scales,
+                                         int grow, const AttnParams& p, int h) {
+  const uint8_t* crow = codes + ((size_t)grow * p.H + h) * (D / 2);
+  const uint8_t* srow = scales + ((size_t)grow * p.H + h) * (D / 16);
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) raw.c[q] = *reinterpret_cast<const uint4*>(crow + q * 16);
+  if constexpr (D == 128) {
+    const uint2 s8 = *reinterpret_cast<const uint2*>(srow);
+    raw.s[0] = s8.x;
+    raw.s[1] = s8.y;
+  } else {
+    raw.s[0] = *reinterpret_cast<const uint32_t*>(srow);
+  }
+}
+
 // Exact partial decode e2m1(code) * e4m3(scale): at most 6 significant bits
 // and a range of [2^-10, 2688], so the product is exact in f16 and in bf16.
 // The fp32 tensor scale of the region is applied by the softmax instead (K: in
 // the logit scale, V: folded into P), so no tile value is rounded here.
+// Thread r writes key row r in the 128-byte-swizzled layout of the MMA operands.
 template <int D, bool kHalfOut>
-__device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r, int grow,
-                                            bool live, const uint8_t* codes, const uint8_t* scales,
-                                            const AttnParams& p, int h) {
+__device__ __forceinline__ void decode_row(__nv_bfloat16 (*dst)[BN * 64], int r, bool live,
+                                           const RawRow<D>& raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>(dst);
   if (!live) {
 #pragma unroll
@@ -185,26 +208,14 @@ __device__ __forceinline__ void dequant_row(__nv_bfloat16 (*dst)[BN * 64], int r
     }
     return;
   }
-  const uint8_t* crow = codes + ((size_t)grow * p.H + h) * (D / 2);
-  const uint8_t* srow = scales + ((size_t)grow * p.H + h) * (D / 16);
-  uint32_t sc[D / 16];
-  if constexpr (D == 128) {
-    const uint2 s8 = *reinterpret_cast<const uint2*>(srow);
-    const uint32_t sw[2] = {s8.x, s8.y};
-#pragma unroll
-    for (int b = 0; b < 8; ++b) sc[b] = (sw[b >> 2] >> (8 * (b & 3))) & 0xFFu;
-  } else {
-    const uint32_t s4 = *reinterpret_cast<const uint32_t*>(srow);
-#pragma unroll
-    for (int b = 0; b < 4; ++b) sc[b] = (s4 >> (8 * b)) & 0xFFu;
-  }
 #pragma unroll
   for (int q16 = 0; q16 < D / 32; ++q16) {  // 16 code bytes = 32 elements = 2 blocks
-    const uint4 cw = *reinterpret_cast<const uint4*>(crow + q16 * 16);
-    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t w[4] = {raw.c[q16].x, raw.c[q16].y, raw.c[q16].z, raw.c[q16].w};
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // one 16-element block -> two 16-byte chunks
-      const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc[q16 * 2 + half]));  // exact
+      const int b = q16 * 2 + half;
+      const uint32_t sc = (raw.s[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+      const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc));  // exact
       uint32_t outw[8];
 #pragma unroll
       for (int bi = 0; bi < 8; ++bi) {
@@ -359,25 +370,41 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       const int h = pc.u / p.n_pairs;
       KvCursor cur;
       cur.seek(p, Share::first_tile(p, pc));
+      RawRow<D> rk, rv;
+      bool live = r < cur.valid(p);
+      if (live) {
+        load_raw<D>(rk, p.kc, p.ks, cur.row0(p) + r, p, h);
+        load_raw<D>(rv, p.vc, p.vs, cur.row0(p) + r, p, h);
+      }
       for (int t = pc.t0; t < pc.t1; ++t, ++it) {
         const int st = it & 1, n = it >> 1;
-        const int grow = cur.row0(p) + r;
-        const bool live = r < cur.valid(p);
+        // the next tile's codes and scales are in flight while this one decodes
+        KvCursor nxt = cur;
+        nxt.next(p);
+        RawRow<D> nk, nv;
+        const bool nlive = t + 1 < pc.t1 && r < nxt.valid(p);
+        if (nlive) {
+          load_raw<D>(nk, p.kc, p.ks, nxt.row0(p) + r, p, h);
+          load_raw<D>(nv, p.vc, p.vs, nxt.row0(p) + r, p, h);
+        }
         if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
           ok = false;
           break;
         }
-        dequant_row<D, false>(sm.k[st], r, grow, live, p.kc, p.ks, p, h);
+        decode_row<D, false>(sm.k[st], r, live, rk);
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_kfull[st]);
         if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
           ok = false;
           break;
         }
-        dequant_row<D, true>(sm.v[st], r, grow, live, p.vc, p.vs, p, h);
+        decode_row<D, true>(sm.v[st], r, live, rv);
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_vfull[st]);
-        cur.next(p);
+        rk = nk;
+        rv = nv;
+        live = nlive;
+        cur = nxt;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -618,20 +645,27 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           const int region = p.seg[cur.seg].row0 / p.Tc;
           const float cg = c * p.kg[region];
           const float gv = p.vg[region];
-          float mx = -INFINITY;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int j = 0; j < BN / 32; ++j) {
             uint32_t sr[32];
             tmem_ld32(tS + j * 32, sr);
             tmem_ld_wait();
+            if (valid < BN) {  // ragged tile (warp-uniform)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mx = fmax3(mx, j * 32 + e < valid ? __uint_as_float(sr[e]) : -INFINITY,
-                         j * 32 + e + 1 < valid ? __uint_as_float(sr[e + 1]) : -INFINITY);
+              for (int e = 0; e < 32; ++e)
+                if (j * 32 + e >= valid) sr[e] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                m4[q] = fmax3(m4[q], __uint_as_float(sr[e + 2 * q]), __uint_as_float(sr[e + 2 * q + 1]));
           }
+          const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
           const float alpha = decide(i, mx * cg);
-          const float neg = -m_ref;
-          float sum = 0.0f;
+          const uint64_t c2 = f32x2(cg, cg), n2 = f32x2(-m_ref, -m_ref), g2 = f32x2(gv, gv);
+          uint64_t acc2 = f32x2(0.0f, 0.0f);
 #pragma unroll
           for (int j = 0; j < BN / 32; ++j) {
             // chunk j (keys 32j..32j+31) -> P columns 16j..16j+15, which only
@@ -639,19 +673,29 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
             uint32_t sr[32];
             tmem_ld32(tS + j * 32, sr);
             tmem_ld_wait();
+            if (valid < BN) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (j * 32 + e >= valid) sr[e] = __float_as_uint(-INFINITY);
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int k0 = j * 32 + 2 * e;
-              const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e]), cg, neg)) : 0.0f;
-              const float p1 =
-                  k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), cg, neg)) : 0.0f;
-              sum += p0 + p1;
-              pk[e] = pack_f16x2(p0 * gv, p1 * gv);
+              const uint64_t y2 =
+                  ffma2(f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2, n2);
+              float y0, y1;
+              f32x2_split(y2, y0, y1);
+              const uint64_t p2 = f32x2(ex2_approx(y0), ex2_approx(y1));
+              acc2 = fadd2(acc2, p2);
+              float q0, q1;
+              f32x2_split(fmul2(p2, g2), q0, q1);
+              pk[e] = pack_f16x2(q0, q1);
             }
             tmem_st16(tS + j * 16, pk);
           }
-          l += sum;
+          float s0, s1;
+          f32x2_split(acc2, s0, s1);
+          l += s0 + s1;
           apply(alpha);
         }
         tmem_st_wait();
