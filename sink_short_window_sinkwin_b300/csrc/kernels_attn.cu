@@ -154,12 +154,16 @@ __device__ __forceinline__ Share share_of(const AttnParams& p, int g) {
 // FP4 tile dequantisation: thread i writes key row i of a K or V tile in the
 // 128-byte-swizzled layout the MMA descriptors expect.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
-  return d;
+// 8 E2M1 codes (4 bytes, element 2i in the low nibble of byte i) -> 4 f16x2
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t word, uint32_t (&d)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(word));
 }
 __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
@@ -218,15 +222,18 @@ __device__ __forceinline__ void decode_row(__nv_bfloat16 (*dst)[BN * 64], int r,
       const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc));  // exact
       uint32_t outw[8];
 #pragma unroll
-      for (int bi = 0; bi < 8; ++bi) {
-        const uint32_t word = w[half * 2 + (bi >> 2)];
-        const uint32_t h2 = e2m1x2_to_f16x2((word >> (8 * (bi & 3))) & 0xFFu);
-        const __half2 hv = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);  // exact
-        if constexpr (kHalfOut) {
-          outw[bi] = *reinterpret_cast<const uint32_t*>(&hv);
-        } else {
-          const float2 fv = __half22float2(hv);
-          outw[bi] = pack_bf16x2(fv.x, fv.y);  // exact
+      for (int wi = 0; wi < 2; ++wi) {
+        uint32_t h4[4];
+        e2m1x8_to_f16x8(w[half * 2 + wi], h4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __half2 hv = __hmul2(*reinterpret_cast<const __half2*>(&h4[k]), s2);  // exact
+          if constexpr (kHalfOut) {
+            outw[wi * 4 + k] = *reinterpret_cast<const uint32_t*>(&hv);
+          } else {
+            const float2 fv = __half22float2(hv);
+            outw[wi * 4 + k] = pack_bf16x2(fv.x, fv.y);  // exact
+          }
         }
       }
       const int e0 = q16 * 32 + half * 16;  // first element of this block
@@ -646,7 +653,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           const float cg = c * p.kg[region];
           const float gv = p.vg[region];
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+#pragma unroll 1
           for (int j = 0; j < BN / 32; ++j) {
             uint32_t sr[32];
             tmem_ld32(tS + j * 32, sr);
@@ -666,7 +673,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           const float alpha = decide(i, mx * cg);
           const uint64_t c2 = f32x2(cg, cg), n2 = f32x2(-m_ref, -m_ref), g2 = f32x2(gv, gv);
           uint64_t acc2 = f32x2(0.0f, 0.0f);
-#pragma unroll
+#pragma unroll 1
           for (int j = 0; j < BN / 32; ++j) {
             // chunk j (keys 32j..32j+31) -> P columns 16j..16j+15, which only
             // overlap S columns already consumed
