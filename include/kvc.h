@@ -82,7 +82,9 @@ typedef struct kvc_cache {
   float* k_gscale;   /* FP4 only, [1 + W], else NULL */
   float* v_gscale;   /* FP4 only, [1 + W], else NULL */
   int32_t* dev_ws;   /* KVC_WS_WORDS int32, zero-filled by the caller before kvc_init;
-                        word 0 is the device error word, the rest is reduction scratch */
+                        word 0 is the device error word, the rest is reduction scratch
+                        (the last two words are grid-barrier counters the library keeps
+                        at zero between calls) */
   void* attn_ws;     /* optional attention workspace of kvc_cache_bytes(c, 7) bytes,
                         zero-filled by the caller before first use, or NULL.  With it
                         sinkwin_attn balances work evenly over all SMs (items cut at a

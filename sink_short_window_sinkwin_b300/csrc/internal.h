@@ -22,9 +22,10 @@ struct Seg {
 // dst[i] = src[i] for two tensors of `bytes` bytes each (16-byte aligned, bytes % 16 == 0)
 cudaError_t launch_copy2(void* dst0, const void* src0, void* dst1, const void* src1, size_t bytes,
                          cudaStream_t st);
-// fill two byte ranges with a repeated 16-bit pattern / byte pattern
-cudaError_t launch_fill2_u16(void* d0, void* d1, size_t bytes, uint16_t pattern, cudaStream_t st);
-cudaError_t launch_fill2_u8(void* d0, void* d1, size_t bytes, uint8_t pattern, cudaStream_t st);
+// fill n <= 4 byte ranges (any alignment and length) with a repeated byte pattern
+// given as a 32-bit word (byte i of a 4-byte-aligned group takes byte i of it), one launch
+cudaError_t launch_fill(void* const* dst, const size_t* bytes, const uint32_t* words, int n,
+                        cudaStream_t st);
 
 // FP4 encode of up to two tensors (x1 may be null), n elements each, n % 16 == 0.
 // ws: 2 * kQuantPartials int32 words (per-CTA partial maxima).
@@ -37,6 +38,11 @@ struct QuantJob {
 };
 cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
                              cudaStream_t st);
+// One-pass cooperative encode over `nsm` CTAs (grid barrier on two counters at
+// the end of a cache's device workspace, which must start at zero).
+// cudaErrorNotSupported when the tensors do not fit the CTAs' shared memory.
+cudaError_t launch_quant_fp4_fused(const QuantJob* jobs, int njobs, int64_t n, int32_t* dev_ws,
+                                   int nsm, cudaStream_t st);
 
 // ---- attention (kernels_attn.cu) ----
 struct AttnLaunch {

@@ -37,7 +37,9 @@ constexpr int kStages = 4;
 
 struct GemmParams {
   int32_t rows, HD, Tc;
-  int32_t col0;  // first output column of this launch in [K | V]: 0 (K) or HD (V)
+  int32_t col0;    // first output column of this launch in [K | V]: 0 (K) or HD (V)
+  int32_t ncol;    // column tiles (HD / BN)
+  int32_t ntiles;  // row tiles x column tiles
   int32_t region[kMaxSeg];
   __nv_bfloat16* k;
   __nv_bfloat16* v;
@@ -49,22 +51,26 @@ struct __align__(1024) GemmSmem {
   __nv_bfloat16 a[kStages][RM * RK];
   __nv_bfloat16 b[kStages][BN / 64][RK * 64];
   uint64_t bar_full[kStages], bar_empty[kStages];
-  uint64_t bar_acc, bar_drain;
+  uint64_t bar_acc_full[2], bar_acc_empty[2];  // two TMEM accumulators
+  uint64_t bar_drain;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
+// Persistent: CTA g takes tiles g, g + G, ... (row-major over [row tile][column
+// tile], so consecutive tiles of a CTA share hidden rows through L2).  The
+// accumulator alternates between two TMEM buffers, so the epilogue of one tile
+// overlaps the MMAs of the next.
 // kKf32: K launch (fp32 rows parked in the K|V rows); else the V launch (bf16).
 template <int BN, bool kKf32>
 __global__ void __launch_bounds__(kRThreads, 1)
     recache_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
   using Smem = GemmSmem<BN>;
+  constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nloc = blockIdx.x * BN;  // column within this launch's half
-  const int m0 = blockIdx.y * RM;
   const int nk = p.HD / RK;
 
   if (threadIdx.x == 0) {
@@ -72,13 +78,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
       mbar_init(&sm.bar_full[s], 1);
       mbar_init(&sm.bar_empty[s], 1);
     }
-    mbar_init(&sm.bar_acc, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.bar_acc_full[b], 1);
+      mbar_init(&sm.bar_acc_empty[b], 128);
+    }
     mbar_init(&sm.bar_drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, BN < 32 ? 32 : BN);
+    tmem_alloc(&sm.tmem_base, kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -91,15 +100,21 @@ __global__ void __launch_bounds__(kRThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages, u = kb / kStages;
-        if (kb >= kStages && !mbar_wait(&sm.bar_empty[s], (u - 1) & 1, wd)) break;
-        mbar_expect_tx(&sm.bar_full[s], RM * RK * 2 + RK * BN * 2);
-        tma_load_2d(&sm.a[s][0], &tmA, &sm.bar_full[s], kb * RK, m0);
-        for (int nb = 0; nb < BN / 64; ++nb)
-          tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
-        issued = kb + 1;
+      int issued = 0;  // K-steps loaded by this CTA (ring position)
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        const int m0 = (t / p.ncol) * RM, nloc = (t % p.ncol) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++issued) {
+          const int s = issued % kStages, u = issued / kStages;
+          if (issued >= kStages && !mbar_wait(&sm.bar_empty[s], (u - 1) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.bar_full[s], RM * RK * 2 + RK * BN * 2);
+          tma_load_2d(&sm.a[s][0], &tmA, &sm.bar_full[s], kb * RK, m0);
+          for (int nb = 0; nb < BN / 64; ++nb)
+            tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
+        }
       }
       if (sm.abort_flag) {  // every copy this thread started lands before the CTA exits
         for (int s = 0; s < kStages; ++s) {
@@ -111,23 +126,31 @@ __global__ void __launch_bounds__(kRThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(RM, BN, false, true);
+      int used = 0;  // K-steps consumed (ring position)
+      int j = 0;     // tiles of this CTA
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages, u = kb / kStages;
-        if (!mbar_wait(&sm.bar_full[s], u & 1, wd)) {
-          ok = false;
-          break;
-        }
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++j) {
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait(&sm.bar_acc_empty[buf], ((j >> 1) - 1) & 1, wd)) break;
         tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nk; ++kb, ++used) {
+          const int s = used % kStages, u = used / kStages;
+          if (!mbar_wait(&sm.bar_full[s], u & 1, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < RK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(smem_u32(&sm.a[s][0]) + kk * 32, 0, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(&sm.b[s][0][0]) + kk * 2048, RK * 128, 1024);
-          mma_bf16_ss(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < RK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(smem_u32(&sm.a[s][0]) + kk * 32, 0, 1024);
+            const uint64_t bd = sdesc_sw128(smem_u32(&sm.b[s][0][0]) + kk * 2048, RK * 128, 1024);
+            mma_bf16_ss(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.bar_empty[s]);
         }
-        mma_commit(&sm.bar_empty[s]);
+        if (ok) mma_commit(&sm.bar_acc_full[buf]);
       }
-      if (ok) mma_commit(&sm.bar_acc);
       mma_commit(&sm.bar_drain);  // every MMA issued above completes before TMEM is freed
       mbar_drain(&sm.bar_drain, 0);
     }
@@ -135,23 +158,27 @@ __global__ void __launch_bounds__(kRThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int grow = m0 + r;
-    const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
-    // tcgen05.ld is warp-collective (.sync.aligned): the whole warp loads, and
-    // only the stores are predicated on the row being real (the last row tile
-    // can end inside a warp)
-    if (__all_sync(0xffffffffu, mbar_wait(&sm.bar_acc, 0, wd))) {
+    int j = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++j) {
+      const int buf = j & 1;
+      const int m0 = (t / p.ncol) * RM, nloc = (t % p.ncol) * BN;
+      const uint32_t trow = tmem + (uint32_t)(buf * BN) + ((uint32_t)(wq * 32) << 16);
+      // tcgen05.ld is warp-collective (.sync.aligned): the whole warp loads, and
+      // only the stores are predicated on the row being real (the last row tile
+      // can end inside a warp)
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_acc_full[buf], (j >> 1) & 1, wd))) break;
       tc_fence_after();
+      const int grow = m0 + r;
       const bool live = grow < p.rows;
       const int ci = live ? grow / p.Tc : 0;
       const int64_t dest = (int64_t)p.region[ci] * p.Tc + (grow - ci * p.Tc);
 #pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
+      for (int jj = 0; jj < BN / 32; ++jj) {
         uint32_t x[32];
-        tmem_ld32(trow + j * 32, x);
+        tmem_ld32(trow + jj * 32, x);
         tmem_ld_wait();
         if (!live) continue;
-        const int col = nloc + j * 32;  // column within the half, a multiple of 32
+        const int col = nloc + jj * 32;  // column within the half, a multiple of 32
         if constexpr (kKf32) {
           const int half = p.HD / 2;
           float* row = reinterpret_cast<float*>(col < half ? p.k + dest * p.HD : p.v + dest * p.HD);
@@ -168,6 +195,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
                                pack_bf16x2(__uint_as_float(x[8 * e + 6]), __uint_as_float(x[8 * e + 7])));
         }
       }
+      tc_fence_before();
+      mbar_arrive(&sm.bar_acc_empty[buf]);  // the MMA may reuse this accumulator
     }
   }
 
@@ -176,7 +205,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, BN < 32 ? 32 : BN);
+    tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -267,14 +296,18 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
 }
 
 template <int BN, bool kKf32>
-cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
                         cudaStream_t st) {
   const size_t smem = sizeof(GemmSmem<BN>) + 1024;
   auto kern = recache_gemm_kernel<BN, kKf32>;
   static bool smem_set[64] = {};  // one per instantiation of this launcher
   cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.HD / BN, (rows + RM - 1) / RM);
+  p.ncol = p.HD / BN;
+  p.ntiles = ((rows + RM - 1) / RM) * p.ncol;
+  int nsm = attn_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  const int grid = p.ntiles < nsm ? p.ntiles : nsm;
   kern<<<grid, kRThreads, smem, st>>>(ta, tb, p);
   return cudaGetLastError();
 }

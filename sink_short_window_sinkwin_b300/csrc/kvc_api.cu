@@ -231,7 +231,9 @@ int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64
     QuantJob jobs[2] = {
         {k_chunk, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
         {v_chunk, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
-    e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
+    // one pass over HBM when the chunk fits the SMs' shared memory
+    e = launch_quant_fp4_fused(jobs, 2, n, c->dev_ws, attn_sm_count(), st);
+    if (e == cudaErrorNotSupported) e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
   }
   if (e != cudaSuccess) return KVC_ECUDA;
   c->chunk_of_region[r] = chunk_idx;
@@ -251,16 +253,19 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream) {
     cudaError_t e;
     if (c->dtype == KVC_BF16) {
       const size_t off = (size_t)r * Tc * row_bytes(c, 0);
-      e = launch_fill2_u16(static_cast<uint8_t*>(c->k) + off, static_cast<uint8_t*>(c->v) + off,
-                           (size_t)Tc * row_bytes(c, 0), 0x7FC0u, st);
+      void* d[2] = {static_cast<uint8_t*>(c->k) + off, static_cast<uint8_t*>(c->v) + off};
+      const size_t b[2] = {(size_t)Tc * row_bytes(c, 0), (size_t)Tc * row_bytes(c, 0)};
+      const uint32_t w[2] = {0x7FC07FC0u, 0x7FC07FC0u};  // bf16 NaN
+      e = launch_fill(d, b, w, 2, st);
     } else {
       const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
       const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
-      e = launch_fill2_u8(static_cast<uint8_t*>(c->k) + coff, static_cast<uint8_t*>(c->v) + coff,
-                          (size_t)Tc * row_bytes(c, 0), 0x00u, st);
-      if (e == cudaSuccess)
-        e = launch_fill2_u8(c->k_scale + soff, c->v_scale + soff, (size_t)Tc * row_bytes(c, 2), 0x7Fu,
-                            st);
+      void* d[4] = {static_cast<uint8_t*>(c->k) + coff, static_cast<uint8_t*>(c->v) + coff,
+                    c->k_scale + soff, c->v_scale + soff};
+      const size_t cb = (size_t)Tc * row_bytes(c, 0), sb = (size_t)Tc * row_bytes(c, 2);
+      const size_t b[4] = {cb, cb, sb, sb};
+      const uint32_t w[4] = {0u, 0u, 0x7F7F7F7Fu, 0x7F7F7F7Fu};  // codes 0, scales E4M3 NaN
+      e = launch_fill(d, b, w, 4, st);
     }
     if (e != cudaSuccess) return KVC_ECUDA;
   }
@@ -370,8 +375,13 @@ int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream) {
   int32_t w = 0;
   if (cudaMemcpy(&w, c->dev_ws, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ECUDA;
   if (w != 0) {
-    const int32_t z = 0;
-    if (cudaMemcpy(c->dev_ws, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return KVC_ECUDA;
+    // clear the error word and the encoder's grid-barrier counters (a wait
+    // that ran out can leave them mid-count)
+    const int32_t z[2] = {0, 0};
+    if (cudaMemcpy(c->dev_ws, z, sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->dev_ws + KVC_WS_WORDS - 2, z, 2 * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+      return KVC_ECUDA;
     return KVC_ETIMEOUT;
   }
   return KVC_OK;

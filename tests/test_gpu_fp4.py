@@ -145,3 +145,37 @@ def test_fp4_many_items_full_compare(swl):
             assert_close(to64(out), want, ATOL_FP4, None, f"fp4 228 items step {c}",
                  plus_output_rounding=True)
     assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_fp4_scrub_unaligned_regions(swl):
+    """H=3, D=64, 150-token chunks: a slot's scales span 1800 bytes, so slot
+    boundaries are not 16-byte aligned.  The scrub on evict writes exactly the
+    freed slot (codes 0, scales 0x7F), nothing around it, and attention over the
+    remaining chunks still matches the oracle."""
+    sh = Shapes(3, 64, 50, 3, 2, 1, 50)
+    Tc = sh.chunk_tokens
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, dtype="fp4", scrub_on_evict=True)
+    model = CacheModel(sh.heads, sh.head_dim, Tc, sh.window_chunks)
+    for c in range(3):
+        _, k, v = chunk_qkv(sh, 21, 0, c, "outliers")
+        cache.append(k.cuda(), v.cuda(), c)
+        model.append(c, ofp4.dequantize(*ofp4.quantize(_f32(k))), ofp4.dequantize(*ofp4.quantize(_f32(v))))
+    torch.cuda.synchronize()
+    before = [t.clone() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale)]
+    cache.evict(1)
+    model.evict(1)
+    torch.cuda.synchronize()
+    r = 1  # region of chunk 1
+    sl = slice(r * Tc, (r + 1) * Tc)
+    for t, b, fillv in ((cache.k, before[0], 0), (cache.v, before[1], 0),
+                        (cache.k_scale, before[2], 0x7F), (cache.v_scale, before[3], 0x7F)):
+        assert bool((t[sl] == fillv).all()), "freed slot not scrubbed"
+        assert torch.equal(t[:r * Tc], b[:r * Tc]) and torch.equal(t[(r + 1) * Tc:], b[(r + 1) * Tc:]), \
+            "scrub wrote outside the freed slot"
+    q = chunk_qkv(sh, 22, 0, 3, "rms1", q_rows=70)[0]
+    out = cache.attn(q.cuda(), 1.0 / math.sqrt(64))
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(q), 1.0 / math.sqrt(64))
+    assert_close(to64(out), want, ATOL_FP4, None, "fp4 after unaligned scrub", plus_output_rounding=True)
+    assert cache.last_device_error() == swl.KVC_OK
