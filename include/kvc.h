@@ -82,9 +82,7 @@ typedef struct kvc_cache {
   float* k_gscale;   /* FP4 only, [1 + W], else NULL */
   float* v_gscale;   /* FP4 only, [1 + W], else NULL */
   int32_t* dev_ws;   /* KVC_WS_WORDS int32, zero-filled by the caller before kvc_init;
-                        word 0 is the device error word, the rest is reduction scratch
-                        (the last two words are grid-barrier counters the library keeps
-                        at zero between calls) */
+                        word 0 is the device error word, the rest is reduction scratch */
   void* attn_ws;     /* optional attention workspace of kvc_cache_bytes(c, 7) bytes,
                         zero-filled by the caller before first use, or NULL.  With it
                         sinkwin_attn balances work evenly over all SMs (items cut at a
@@ -160,7 +158,8 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
                     float eps, const int64_t* chunk_ids, int32_t n, int32_t grid_h,
                     int32_t grid_w, float rope_theta, kvc_stream_t stream);
 
-/* FP4-encode n bf16 values (device x, n % 16 == 0, n >= 16) as one tensor:
+/* FP4-encode n finite bf16 values (device x, n % 16 == 0, n >= 16; the codes of
+ * a tensor holding NaN or infinity are unspecified) as one tensor:
  *   amax = max|x|;  g = fl32(amax / 2688);   (g == 0: all codes and scales 0)
  *   per 16-block b: s = E4M3_rne_satfinite(fl32(fl32(amax_b / 6) / g));
  *   s == 0 or fl32(s*g) == 0: codes 0;  else t = fl32(|x| * fl32(1 / fl32(s*g))),

@@ -36,13 +36,10 @@ struct QuantJob {
   uint8_t* scales;
   float* gscale;
 };
+// Two launches: per-CTA partial maxima, then the block encode as a programmatic
+// dependent launch (its first loads overlap the end of the first pass).
 cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
                              cudaStream_t st);
-// One-pass cooperative encode over `nsm` CTAs (grid barrier on two counters at
-// the end of a cache's device workspace, which must start at zero).
-// cudaErrorNotSupported when the tensors do not fit the CTAs' shared memory.
-cudaError_t launch_quant_fp4_fused(const QuantJob* jobs, int njobs, int64_t n, int32_t* dev_ws,
-                                   int nsm, cudaStream_t st);
 
 // ---- attention (kernels_attn.cu) ----
 struct AttnLaunch {

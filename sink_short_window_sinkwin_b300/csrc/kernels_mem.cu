@@ -14,6 +14,7 @@ namespace {
 
 constexpr int kMemThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kFillThreads = 512;
 
 // 128-bit read-only load that does not allocate in L1
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
@@ -24,8 +25,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   return r;
 }
 
-// blockIdx.y picks the tensor; every thread moves kUnroll 16-byte vectors per
-// trip with all loads issued before the stores.
+// blockIdx.y picks the tensor; every thread moves up to kUnroll 16-byte vectors
+// per trip with all loads issued before the stores.
 __global__ void __launch_bounds__(kMemThreads) copy2_kernel(uint4* __restrict__ d0,
                                                             const uint4* __restrict__ s0,
                                                             uint4* __restrict__ d1,
@@ -34,51 +35,66 @@ __global__ void __launch_bounds__(kMemThreads) copy2_kernel(uint4* __restrict__ 
   const uint4* s = blockIdx.y ? s1 : s0;
   uint4* d = blockIdx.y ? d1 : d0;
   const size_t stride = (size_t)gridDim.x * kMemThreads;
-  size_t i = (size_t)blockIdx.x * kMemThreads + threadIdx.x;
-  for (; i + (kUnroll - 1) * stride < n16; i += kUnroll * stride) {
+  // bounds-predicated loads, so the ragged last trip also has all of its loads
+  // in flight at once
+  for (size_t i = (size_t)blockIdx.x * kMemThreads + threadIdx.x; i < n16; i += kUnroll * stride) {
     uint4 r[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) r[u] = ld_nc_v4(s + i + u * stride);
+    for (int u = 0; u < kUnroll; ++u)
+      if (i + u * stride < n16) r[u] = ld_nc_v4(s + i + u * stride);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) d[i + u * stride] = r[u];
+    for (int u = 0; u < kUnroll; ++u)
+      if (i + u * stride < n16) d[i + u * stride] = r[u];
   }
-  for (; i < n16; i += stride) d[i] = ld_nc_v4(s + i);
 }
 
 // Up to four byte ranges, each filled with a repeated byte pattern (given as a
-// 32-bit word); blockIdx.y picks the range (selected, not indexed, so the
-// parameters stay in constant space).  The 16-byte-aligned body is written
-// with vector stores, the head and tail bytes by the first CTA of the range.
+// 32-bit word).  The 16-byte-aligned bodies of the ranges form one index
+// space of vectors (range r holds vectors [s[r], s[r+1])), so one grid-stride
+// loop sized to a single wave covers all of them; the range of a vector is
+// picked by comparisons and selects (the parameters stay in constant space).
+// The at most 15 head and 15 tail bytes of range r are written by warp r of
+// the first CTA.
 struct FillJobs {
-  uint8_t* d[4];
-  size_t bytes[4];
+  uint4* body[4];
+  uint8_t* head[4];  // [head, body) and [tail, end) are the unaligned bytes
+  uint8_t* tail[4];
+  uint8_t* end[4];
+  uint64_t s[5];  // vector prefix sums of the bodies
   uint32_t word[4];
 };
-__global__ void __launch_bounds__(kMemThreads) fill_kernel(FillJobs f) {
-  const int y = blockIdx.y;
-  uint8_t* d = y == 0 ? f.d[0] : y == 1 ? f.d[1] : y == 2 ? f.d[2] : f.d[3];
-  const size_t n = y == 0 ? f.bytes[0] : y == 1 ? f.bytes[1] : y == 2 ? f.bytes[2] : f.bytes[3];
-  const uint32_t word = y == 0 ? f.word[0] : y == 1 ? f.word[1] : y == 2 ? f.word[2] : f.word[3];
-  const uintptr_t p0 = reinterpret_cast<uintptr_t>(d), p1 = p0 + n;
-  uintptr_t a = (p0 + 15) & ~uintptr_t(15), e = p1 & ~uintptr_t(15);
-  if (a > e) a = e = p1;  // shorter than one aligned vector: all head bytes
-  uint4* body = reinterpret_cast<uint4*>(a);
-  const size_t n16 = (e - a) / 16;
-  const uint4 w = make_uint4(word, word, word, word);
-  const size_t stride = (size_t)gridDim.x * kMemThreads;
-  for (size_t i = (size_t)blockIdx.x * kMemThreads + threadIdx.x; i < n16; i += stride) body[i] = w;
-  if (blockIdx.x == 0 && threadIdx.x < 32) {  // at most 15 head and 15 tail bytes
-    const uintptr_t h = p0 + threadIdx.x, t = e + threadIdx.x;
-    if (h < a) *reinterpret_cast<uint8_t*>(h) = (uint8_t)(word >> (8 * (h & 3)));
-    if (t < p1) *reinterpret_cast<uint8_t*>(t) = (uint8_t)(word >> (8 * (t & 3)));
+template <typename T>
+__device__ __forceinline__ T pick4(int r, T a, T b, T c, T d) {
+  return r == 0 ? a : r == 1 ? b : r == 2 ? c : d;
+}
+__global__ void __launch_bounds__(kFillThreads) fill_kernel(FillJobs f) {
+  const uint64_t total = f.s[4];
+  const uint64_t stride = (uint64_t)gridDim.x * kFillThreads;
+  for (uint64_t i = (uint64_t)blockIdx.x * kFillThreads + threadIdx.x; i < total; i += stride) {
+    const int r = (int)(i >= f.s[1]) + (int)(i >= f.s[2]) + (int)(i >= f.s[3]);
+    uint4* d = pick4(r, f.body[0], f.body[1], f.body[2], f.body[3]);
+    const uint32_t w = pick4(r, f.word[0], f.word[1], f.word[2], f.word[3]);
+    d[i - pick4(r, f.s[0], f.s[1], f.s[2], f.s[3])] = make_uint4(w, w, w, w);
+  }
+  const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && r < 4) {
+    const uint32_t w = pick4(r, f.word[0], f.word[1], f.word[2], f.word[3]);
+    uint8_t* h = pick4(r, f.head[0], f.head[1], f.head[2], f.head[3]) + lane;
+    uint8_t* t = pick4(r, f.tail[0], f.tail[1], f.tail[2], f.tail[3]) + lane;
+    if (h < reinterpret_cast<uint8_t*>(pick4(r, f.body[0], f.body[1], f.body[2], f.body[3])))
+      *h = (uint8_t)(w >> (8 * (reinterpret_cast<uintptr_t>(h) & 3)));
+    if (t < pick4(r, f.end[0], f.end[1], f.end[2], f.end[3]))
+      *t = (uint8_t)(w >> (8 * (reinterpret_cast<uintptr_t>(t) & 3)));
   }
 }
 
-int mem_grid(size_t n16) {
-  // enough CTAs for ~kUnroll vectors per thread, capped at 8 waves of 148 SMs
+// CTAs per tensor of a copy: about kUnroll vectors per thread, and at most one
+// wave of 8 CTAs per SM over all `ny` tensors
+int mem_grid(size_t n16, int ny) {
   size_t want = (n16 + (size_t)kMemThreads * kUnroll - 1) / ((size_t)kMemThreads * kUnroll);
+  const size_t wave = (size_t)attn_sm_count() * 8 / (size_t)ny;
+  if (want > wave) want = wave;
   if (want < 1) want = 1;
-  if (want > 148 * 8) want = 148 * 8;
   return (int)want;
 }
 
@@ -88,16 +104,6 @@ int mem_grid(size_t n16) {
 struct QuantJobs {
   QuantJob j[2];
 };
-
-// max |x| over bf16 bits: clearing the sign bit leaves bit patterns whose
-// unsigned order is the order of the magnitudes (finite inputs)
-__device__ __forceinline__ uint32_t absmax_bf16x8(uint4 v, uint32_t acc2) {
-  acc2 = __vmaxu2(acc2, v.x & 0x7FFF7FFFu);
-  acc2 = __vmaxu2(acc2, v.y & 0x7FFF7FFFu);
-  acc2 = __vmaxu2(acc2, v.z & 0x7FFF7FFFu);
-  acc2 = __vmaxu2(acc2, v.w & 0x7FFF7FFFu);
-  return acc2;
-}
 
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   v = __reduce_max_sync(0xffffffffu, v);
@@ -115,31 +121,6 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   return v;
 }
 
-// Pass 1: every CTA writes the magnitude maximum of its grid-stride share as
-// bf16 bits into its own scratch word (no atomics, no zeroing needed).
-__global__ void __launch_bounds__(kMemThreads) amax_kernel(QuantJobs jobs, int64_t n,
-                                                           int32_t* __restrict__ ws) {
-  __shared__ uint32_t red[32];
-  // select, not index: a dynamic index would copy the parameter struct to local memory
-  const uint4* x = reinterpret_cast<const uint4*>(blockIdx.y ? jobs.j[1].x : jobs.j[0].x);
-  const int64_t n8 = n >> 3;
-  uint32_t acc2 = 0;
-  const int64_t stride = (int64_t)gridDim.x * kMemThreads;
-  int64_t i = (int64_t)blockIdx.x * kMemThreads + threadIdx.x;
-  for (; i + 3 * stride < n8; i += 4 * stride) {
-    uint4 r0 = ld_nc_v4(x + i), r1 = ld_nc_v4(x + i + stride), r2 = ld_nc_v4(x + i + 2 * stride),
-          r3 = ld_nc_v4(x + i + 3 * stride);
-    acc2 = absmax_bf16x8(r0, acc2);
-    acc2 = absmax_bf16x8(r1, acc2);
-    acc2 = absmax_bf16x8(r2, acc2);
-    acc2 = absmax_bf16x8(r3, acc2);
-  }
-  for (; i < n8; i += stride) acc2 = absmax_bf16x8(ld_nc_v4(x + i), acc2);
-  uint32_t m = max(acc2 & 0xFFFFu, acc2 >> 16);
-  m = block_max_u32(m, red);
-  if (threadIdx.x == 0) ws[blockIdx.y * kQuantPartials + blockIdx.x] = (int32_t)m;
-}
-
 // E4M3 code of x >= 0, round to nearest even, saturating at 448 (the
 // hardware conversion; OCP E4M3: bias 7, subnormal quantum 2^-9)
 __device__ __forceinline__ uint32_t e4m3_rne_satfinite(float x) {
@@ -152,16 +133,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
   if (e == 0) return (float)m * 0.001953125f;             // m * 2^-9
   return __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
-}
-
-// Two E2M1 codes (sign | magnitude, round to nearest even, saturating at 6):
-// lo in the low nibble.  The sign of a value that rounds to 0 is kept.
-__device__ __forceinline__ uint32_t e2m1x2_rne_satfinite(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -190,205 +161,197 @@ __device__ __forceinline__ float div6_bf16(float a) {
   return __fmaf_rn(e, r, q);
 }
 
-// One 16-element block (8 words of bf16 pairs) under tensor scale g: its E4M3
-// scale byte and 8 bytes of packed E2M1 codes, in the fixed fp32 order of the
-// encode rule.
-__device__ __forceinline__ void encode_block(const uint32_t (&w)[8], float g, const ScaleTab& tab,
-                                             uint32_t& s, uint32_t& lo, uint32_t& hi) {
-  uint32_t acc2 = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) acc2 = __vmaxu2(acc2, w[k] & 0x7FFF7FFFu);
-  const float amax_b = __uint_as_float(max(acc2 & 0xFFFFu, acc2 >> 16) << 16);
+// Eight E2M1 codes (four RNE-satfinite pair conversions) packed into one word,
+// element 0 in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x8_rne_satfinite(float a0, float a1, float a2, float a3,
+                                                         float a4, float a5, float a6, float a7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+  return r;
+}
+
+// max(|a|, |b|) per bf16 lane (the sign bit of the result is the XOR of the
+// operands' signs, which the callers mask off)
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16 magnitude bits of the largest |x| over a 16-element block (finite x)
+__device__ __forceinline__ uint32_t block_amax_bits(const uint32_t (&w)[8]) {
+  const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(bf16x2_max_abs(w[0], w[1]), bf16x2_max_abs(w[2], w[3])),
+                                    bf16x2_max_abs(bf16x2_max_abs(w[4], w[5]), bf16x2_max_abs(w[6], w[7]))) &
+                     0x7FFF7FFFu;
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// One 16-element block (8 words of bf16 pairs, block amax given as bf16
+// magnitude bits) under tensor scale g: its E4M3 scale byte and 8 bytes of
+// packed E2M1 codes, in the fixed fp32 order of the encode rule.
+__device__ __forceinline__ void encode_block_amax(const uint32_t (&w)[8], uint32_t amax_bits, float g,
+                                                  const ScaleTab& tab, uint32_t& s, uint32_t& lo,
+                                                  uint32_t& hi) {
   s = 0;
   lo = 0;
   hi = 0;
   if (g == 0.0f) return;
-  s = e4m3_rne_satfinite(__fdiv_rn(div6_bf16(amax_b), g));
+  s = e4m3_rne_satfinite(__fdiv_rn(div6_bf16(__uint_as_float(amax_bits << 16)), g));
   const float2 sgi = tab.e[s];  // {s * g, 1 / (s * g)}
   if (s == 0 || sgi.x == 0.0f) {
     s = 0;
     return;
   }
-  const float inv = sgi.y;
-  // |x| * inv and x * inv round to the same magnitude; the sign rides along
+  const uint64_t inv2 = f32x2(sgi.y, sgi.y);
+  // |x| * inv and x * inv round to the same magnitude; the sign rides along.
+  // Both elements of a word are scaled by one packed (per-lane IEEE) multiply.
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t byte =
-        e2m1x2_rne_satfinite(__fmul_rn(bf16_lo(w[k]), inv), __fmul_rn(bf16_hi(w[k]), inv));
-    if (k < 4) lo |= byte << (8 * k);
-    else hi |= byte << (8 * (k - 4));
+  for (int h = 0; h < 2; ++h) {
+    float y[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      f32x2_split(fmul2(f32x2(bf16_lo(w[4 * h + k]), bf16_hi(w[4 * h + k])), inv2), y[2 * k], y[2 * k + 1]);
+    (h ? hi : lo) = e2m1x8_rne_satfinite(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
   }
 }
 
-// Pass 2: tensor scale from the partial maxima, then one thread per 16-element
-// block: its E4M3 scale byte and 8 bytes of packed E2M1 codes.
-__global__ void __launch_bounds__(kMemThreads) quant_kernel(QuantJobs jobs, int64_t n,
-                                                            const int32_t* __restrict__ ws) {
-  __shared__ uint32_t red[32];
-  const QuantJob job = blockIdx.y ? jobs.j[1] : jobs.j[0];
-  uint32_t m = 0;
-  for (int i = threadIdx.x; i < kQuantPartials; i += kMemThreads)
-    m = max(m, (uint32_t)ws[blockIdx.y * kQuantPartials + i]);
-  m = block_max_u32(m, red);
-  const float amax = __uint_as_float(m << 16);
-  const float g = __fdiv_rn(amax, 2688.0f);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *job.gscale = g;
-  __shared__ ScaleTab tab;
-  build_scale_tab(tab, g, threadIdx.x, kMemThreads);
-  __syncthreads();
-
-  const uint4* x = reinterpret_cast<const uint4*>(job.x);
-  uint2* codes = reinterpret_cast<uint2*>(job.codes);
-  const int64_t nblk = n >> 4;
-  const int64_t stride = (int64_t)gridDim.x * kMemThreads;
-  for (int64_t b = (int64_t)blockIdx.x * kMemThreads + threadIdx.x; b < nblk; b += stride) {
-    const uint4 v0 = ld_nc_v4(x + 2 * b), v1 = ld_nc_v4(x + 2 * b + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t s, lo, hi;
-    encode_block(w, g, tab, s, lo, hi);
-    codes[b] = make_uint2(lo, hi);
-    job.scales[b] = (uint8_t)s;
-  }
+__device__ __forceinline__ void encode_block(const uint32_t (&w)[8], float g, const ScaleTab& tab,
+                                             uint32_t& s, uint32_t& lo, uint32_t& hi) {
+  encode_block_amax(w, block_amax_bits(w), g, tab, s, lo, hi);
 }
 
 // ---------------------------------------------------------------------------
-// FP4 encode in one pass over HBM (cooperative; used by the FP4 append)
+// FP4 encode in two passes; the second runs as a programmatic dependent launch
 // ---------------------------------------------------------------------------
-// Every CTA (one per SM) parks its contiguous share of the 16-element blocks
-// of both tensors in shared memory with one or two bulk copies, takes the
-// partial magnitude maxima, meets the other CTAs at a grid barrier (bounded
-// wait on an arrival counter in the cache's device workspace), derives the
-// tensor scales from all partials, and encodes its blocks from shared memory.
-// The input is read from HBM once.  The last CTA to leave resets the
-// counters, so each launch starts from zero (the workspace is zero-filled at
-// kvc_init and kvc_last_device_error clears the counters after an error).
-constexpr int kFusedThreads = 1024;
-constexpr int kFusedMaxBlocks = 6912;  // 216 KiB of parked blocks per CTA
-constexpr int kCntArrive = KVC_WS_WORDS - 2;
-constexpr int kCntDepart = KVC_WS_WORDS - 1;
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+// The encode pass re-reads the input the amax pass just streamed; a K/V chunk
+// (2 x 14.4 MB for the LongLive-1.3B layer shape) fits the 126 MB L2.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-__device__ __forceinline__ int32_t ld_acquire_gpu_s32(const int32_t* a) {
-  int32_t v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
-  return v;
+// wait until the previous grid in the stream has completed and its memory is visible
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint4 v) {
+  return bf16x2_max_abs(acc, bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w)));
 }
 
-__global__ void __launch_bounds__(kFusedThreads, 1)
-    quant_fused_kernel(QuantJobs jobs, int njobs, int64_t nb, int32_t* __restrict__ dev_ws) {
-  extern __shared__ uint4 park[];  // [blocks][2]
-  __shared__ uint64_t bar;
+// Pass 1: CTA (x, j) takes a contiguous range of tensor j's 16-byte vectors and
+// writes the range's magnitude maximum (bf16 bits) to ws[j * kQuantPartials + x]
+// (no atomics, nothing to zero).  Two CTAs per SM, six loads in flight per
+// thread on every trip.
+constexpr int kAmaxThreads = 1024;
+constexpr int kAmaxUnroll = 6;
+__global__ void __launch_bounds__(kAmaxThreads, 2) amax_kernel(QuantJobs jobs, int64_t n,
+                                                               int32_t* __restrict__ ws) {
+  pdl_launch_dependents();  // the encode pass may take the SM slots this grid frees
   __shared__ uint32_t red[32];
-  __shared__ float gsh[2];
-  __shared__ ScaleTab tabs[2];
-  __shared__ int32_t abort_flag;
-  const int G = gridDim.x, g = blockIdx.x, tid = threadIdx.x;
-  int32_t* part = dev_ws + 1;  // [2][G] partial maxima (bf16 magnitude bits)
-  const int64_t T = nb * njobs;
-  const int64_t b0 = (int64_t)g * T / G, b1 = (int64_t)(g + 1) * T / G;
-  const int cnt = (int)(b1 - b0);
-  const int j0 = (int)(b0 / nb);
-  const int c0 = (int)min((int64_t)cnt, (int64_t)(j0 + 1) * nb - b0);  // blocks of job j0
-  const QuantJob ja = j0 ? jobs.j[1] : jobs.j[0];
-  const QuantJob jb = jobs.j[1];
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    abort_flag = 0;
-    fence_mbar_init();
+  // select, not index: a dynamic index would copy the parameter struct to local memory
+  const uint4* x = reinterpret_cast<const uint4*>(blockIdx.y ? jobs.j[1].x : jobs.j[0].x);
+  const int64_t n8 = n >> 3, G = gridDim.x;
+  const int64_t v1 = ((int64_t)blockIdx.x + 1) * n8 / G;
+  uint32_t acc = 0;
+  // every trip issues all of its (bounds-predicated) loads before using any,
+  // the ragged last trip included
+  for (int64_t i = (int64_t)blockIdx.x * n8 / G + threadIdx.x; i < v1; i += kAmaxUnroll * kAmaxThreads) {
+    uint4 r[kAmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u)
+      r[u] = i + u * kAmaxThreads < v1 ? ld_nc_v4(x + i + u * kAmaxThreads) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) acc = absmax_acc(acc, r[u]);
   }
-  __syncthreads();
-  const Watchdog wd{&abort_flag, dev_ws};
-  if (tid == 0 && cnt > 0) {
-    mbar_expect_tx(&bar, (uint32_t)cnt * 32u);
-    bulk_g2s(park, static_cast<const uint8_t*>(ja.x) + (b0 - (int64_t)j0 * nb) * 32, (uint32_t)c0 * 32u, &bar);
-    if (cnt > c0) bulk_g2s(park + 2 * c0, jb.x, (uint32_t)(cnt - c0) * 32u, &bar);
-  }
-  // block-uniform (a __syncthreads below depends on it)
-  const bool landed = __syncthreads_and(cnt == 0 || mbar_wait(&bar, 0, wd)) != 0;
-  // partial maxima of the (at most two) tensors this share touches
-  uint32_t a0 = 0, a1 = 0;
-  if (landed) {
-    for (int i = tid; i < cnt; i += kFusedThreads) {
-      const int f = (i >> 2) & 1;  // bank-group order, as in the encode loop
-      const uint32_t m = absmax_bf16x8(park[2 * i + 1 - f], absmax_bf16x8(park[2 * i + f], 0u));
-      if (i < c0) a0 = __vmaxu2(a0, m);
-      else a1 = __vmaxu2(a1, m);
+  acc &= 0x7FFF7FFFu;
+  const uint32_t m = block_max_u32(max(acc & 0xFFFFu, acc >> 16), red);
+  if (threadIdx.x == 0) ws[blockIdx.y * kQuantPartials + blockIdx.x] = (int32_t)m;
+}
+
+// Pass 2: CTA (x, j) encodes a contiguous range of tensor j's 16-element
+// blocks: blocks i and i + kEncThreads of the range per thread and trip, the
+// next pair's loads in flight while the current pair is encoded (two register
+// sets used in turn).  The first pair is read before waiting on the amax pass
+// (it is input, not written by that pass); the tensor scale then comes from
+// that pass's `parts` partial maxima.
+constexpr int kEncThreads = 512;
+struct BlockPair {
+  uint4 v[4];
+};
+__device__ __forceinline__ void load_pair(const uint4* x, int i, int cnt, BlockPair& r) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int b = i + h * kEncThreads;
+    if (b < cnt) {
+      r.v[2 * h] = ld_nc_v4(x + 2 * b);
+      r.v[2 * h + 1] = ld_nc_v4(x + 2 * b + 1);
     }
   }
-  const uint32_t m0 = block_max_u32(max(a0 & 0xFFFFu, a0 >> 16), red);
-  const uint32_t m1 = block_max_u32(max(a1 & 0xFFFFu, a1 >> 16), red);
-  if (tid == 0) {
-    part[g] = (int32_t)(j0 == 0 ? m0 : 0u);
-    part[G + g] = (int32_t)(j0 == 0 ? m1 : m0);
-    __threadfence();
-    atomicAdd(dev_ws + kCntArrive, 1);
-    // grid barrier: every CTA of this cooperative launch is resident
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu_s32(dev_ws + kCntArrive) < G) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        abort_flag = 1;
-        atomicCAS(dev_ws, DEVERR_NONE, DEVERR_TIMEOUT);
-        break;
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (!abort_flag && landed) {
-    // tensor scale of each tensor from all G partial maxima (warp j: tensor j)
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp < njobs) {
-      uint32_t m = 0;
-      for (int i = lane; i < G; i += 32) m = max(m, (uint32_t)part[warp * G + i]);
-      m = __reduce_max_sync(0xffffffffu, m);
-      if (lane == 0) gsh[warp] = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
-    }
-    __syncthreads();
-    if (g == 0 && tid < njobs) *(tid ? jobs.j[1].gscale : jobs.j[0].gscale) = gsh[tid];
-    for (int j = 0; j < njobs; ++j) build_scale_tab(tabs[j], gsh[j], tid, kFusedThreads);
-    __syncthreads();
-    for (int i = tid; i < cnt; i += kFusedThreads) {
-      const bool first = i < c0;
-      const int j = first ? j0 : j0 + 1;
-      const QuantJob& jo = first ? ja : jb;
-      const int64_t lb = b0 + i - (int64_t)j * nb;  // block within its tensor
-      // the two 16-byte halves are read in an order that keeps the 8 lanes of
-      // a quarter-warp on 8 different bank groups
-      const int f = (i >> 2) & 1;
-      const uint4 va = park[2 * i + f], vb = park[2 * i + 1 - f];
-      const uint4 v0 = f ? vb : va, v1 = f ? va : vb;
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+}
+__device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, float g, const ScaleTab& tab,
+                                            uint2* codes, uint8_t* scales) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int b = i + h * kEncThreads;
+    if (b < cnt) {
+      const uint32_t w[8] = {r.v[2 * h].x,     r.v[2 * h].y,     r.v[2 * h].z,     r.v[2 * h].w,
+                             r.v[2 * h + 1].x, r.v[2 * h + 1].y, r.v[2 * h + 1].z, r.v[2 * h + 1].w};
       uint32_t sc, lo, hi;
-      encode_block(w, gsh[j], tabs[j], sc, lo, hi);
-      reinterpret_cast<uint2*>(jo.codes)[lb] = make_uint2(lo, hi);
-      jo.scales[lb] = (uint8_t)sc;
-    }
-  } else if (tid == 0 && cnt > 0 && !landed) {
-    mbar_drain(&bar, 0);  // the bulk copies land before the CTA exits
-  }
-  // leave; the last CTA out resets the counters for the next launch
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(dev_ws + kCntDepart, 1) == G - 1) {
-      atomicExch(dev_ws + kCntArrive, 0);
-      atomicExch(dev_ws + kCntDepart, 0);
+      encode_block(w, g, tab, sc, lo, hi);
+      codes[b] = make_uint2(lo, hi);
+      scales[b] = (uint8_t)sc;
     }
   }
 }
+__global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, int64_t n,
+                                                               const int32_t* __restrict__ ws,
+                                                               int parts) {
+  __shared__ uint32_t red[32];
+  __shared__ float gsh;
+  __shared__ ScaleTab tab;
+  const QuantJob job = blockIdx.y ? jobs.j[1] : jobs.j[0];
+  const int tid = threadIdx.x;
+  const int64_t nb = n >> 4, G = gridDim.x;
+  const int64_t b0 = (int64_t)blockIdx.x * nb / G;
+  const int cnt = (int)(((int64_t)blockIdx.x + 1) * nb / G - b0);  // blocks of this CTA
+  const uint4* x = reinterpret_cast<const uint4*>(job.x) + 2 * b0;
+  uint2* codes = reinterpret_cast<uint2*>(job.codes) + b0;
+  uint8_t* scales = job.scales + b0;
+  BlockPair A, B;
+  int i = tid;
+  load_pair(x, i, cnt, A);
+  pdl_wait();  // the amax pass's partial maxima are complete and visible
+  uint32_t m = 0;
+  for (int k = tid; k < parts; k += kEncThreads) m = max(m, (uint32_t)__ldcg(ws + blockIdx.y * kQuantPartials + k));
+  m = block_max_u32(m, red);
+  if (tid == 0) gsh = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+  __syncthreads();
+  const float g = gsh;
+  if (blockIdx.x == 0 && tid == 0) *job.gscale = g;
+  build_scale_tab(tab, g, tid, kEncThreads);
+  __syncthreads();
+  while (i < cnt) {
+    load_pair(x, i + 2 * kEncThreads, cnt, B);
+    encode_pair(A, i, cnt, g, tab, codes, scales);
+    i += 2 * kEncThreads;
+    if (i >= cnt) break;
+    load_pair(x, i + 2 * kEncThreads, cnt, A);
+    encode_pair(B, i, cnt, g, tab, codes, scales);
+    i += 2 * kEncThreads;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_copy2(void* dst0, const void* src0, void* dst1, const void* src1, size_t bytes,
                          cudaStream_t st) {
   const size_t n16 = bytes / 16;
   if (n16 == 0) return cudaSuccess;
-  dim3 grid(mem_grid(n16), dst1 ? 2 : 1);
+  dim3 grid(mem_grid(n16, dst1 ? 2 : 1), dst1 ? 2 : 1);
   copy2_kernel<<<grid, kMemThreads, 0, st>>>(
       static_cast<uint4*>(dst0), static_cast<const uint4*>(src0), static_cast<uint4*>(dst1),
       static_cast<const uint4*>(src1), n16);
@@ -398,64 +361,64 @@ cudaError_t launch_copy2(void* dst0, const void* src0, void* dst1, const void* s
 cudaError_t launch_fill(void* const* dst, const size_t* bytes, const uint32_t* words, int n,
                         cudaStream_t st) {
   if (n < 1 || n > 4) return cudaErrorInvalidValue;
+  size_t any = 0;
+  for (int r = 0; r < n; ++r) any |= bytes[r];
+  if (any == 0) return cudaSuccess;
   FillJobs f{};
-  size_t most = 0;
-  for (int i = 0; i < n; ++i) {
-    f.d[i] = static_cast<uint8_t*>(dst[i]);
-    f.bytes[i] = bytes[i];
-    f.word[i] = words[i];
-    most = bytes[i] > most ? bytes[i] : most;
+  for (int r = 0; r < 4; ++r) {
+    // unused ranges: empty, at the first range's start
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(dst[r < n ? r : 0]);
+    const uintptr_t p1 = p0 + (r < n ? bytes[r] : 0);
+    uintptr_t a = (p0 + 15) & ~uintptr_t(15), e = p1 & ~uintptr_t(15);
+    if (a > e) a = e = p1;  // shorter than one aligned vector: all head bytes
+    f.head[r] = reinterpret_cast<uint8_t*>(p0);
+    f.body[r] = reinterpret_cast<uint4*>(a);
+    f.tail[r] = reinterpret_cast<uint8_t*>(e);
+    f.end[r] = reinterpret_cast<uint8_t*>(p1);
+    f.word[r] = r < n ? words[r] : 0u;
+    f.s[r + 1] = f.s[r] + (e - a) / 16;
   }
-  if (most == 0) return cudaSuccess;
-  fill_kernel<<<dim3(mem_grid(most / 16 + 1), n), kMemThreads, 0, st>>>(f);
+  const uint64_t total = f.s[4];
+  // a single wave: at most 4 CTAs of 512 threads per SM, about 8 vectors a thread
+  uint64_t ctas = (total + (uint64_t)kFillThreads * 8 - 1) / ((uint64_t)kFillThreads * 8);
+  const uint64_t wave = (uint64_t)attn_sm_count() * 4;
+  if (ctas > wave) ctas = wave;
+  if (ctas < 1) ctas = 1;
+  fill_kernel<<<(unsigned)ctas, kFillThreads, 0, st>>>(f);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
                              cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
+  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
   QuantJobs qj{};
   for (int i = 0; i < njobs; ++i) qj.j[i] = jobs[i];
-  amax_kernel<<<dim3(kQuantPartials, njobs), kMemThreads, 0, st>>>(qj, n, ws);
+  const int nsm = attn_sm_count();
+  // pass 1: two 1024-thread CTAs per SM over all tensors
+  int parts = 2 * nsm / njobs;
+  if (parts > kQuantPartials) parts = kQuantPartials;
+  const int64_t n8 = n >> 3;
+  if (parts > n8) parts = (int)n8;
+  amax_kernel<<<dim3(parts, njobs), kAmaxThreads, 0, st>>>(qj, n, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t nblk = n >> 4;
-  int64_t want = (nblk + kMemThreads - 1) / kMemThreads;
-  if (want > 148 * 8) want = 148 * 8;
-  if (want < 1) want = 1;
-  quant_kernel<<<dim3((unsigned)want, njobs), kMemThreads, 0, st>>>(qj, n, ws);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant_fp4_fused(const QuantJob* jobs, int njobs, int64_t n, int32_t* dev_ws,
-                                   int nsm, cudaStream_t st) {
-  if (n <= 0) return cudaSuccess;
+  // pass 2: two 512-thread CTAs per SM over all tensors, as a dependent launch
+  int64_t ctas = 2 * (int64_t)nsm / njobs;
   const int64_t nb = n >> 4;
-  const int64_t T = nb * njobs;
-  const int G = nsm;
-  if (njobs < 1 || njobs > 2 || G < 1 || 1 + 2 * G >= kCntArrive) return cudaErrorNotSupported;
-  const int64_t per = (T + G - 1) / G;
-  if (per > kFusedMaxBlocks || T < G) return cudaErrorNotSupported;
-  for (int i = 0; i < njobs; ++i)
-    if ((reinterpret_cast<uintptr_t>(jobs[i].x) & 15u) || (reinterpret_cast<uintptr_t>(jobs[i].codes) & 7u))
-      return cudaErrorNotSupported;
-  QuantJobs qj{};
-  for (int i = 0; i < njobs; ++i) qj.j[i] = jobs[i];
-  const size_t smem = (size_t)per * 32;
-  static bool smem_set[64] = {};
-  cudaError_t e = set_smem_once(quant_fused_kernel, (size_t)kFusedMaxBlocks * 32, smem_set);
-  if (e != cudaSuccess) return e;
+  if (ctas > (nb + kEncThreads - 1) / kEncThreads) ctas = (nb + kEncThreads - 1) / kEncThreads;
+  if (ctas < 1) ctas = 1;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(G, 1, 1);
-  cfg.blockDim = dim3(kFusedThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3((unsigned)ctas, (unsigned)njobs, 1);
+  cfg.blockDim = dim3(kEncThreads, 1, 1);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quant_fused_kernel, qj, njobs, nb, dev_ws);
+  return cudaLaunchKernelEx(&cfg, quant_kernel, qj, n, static_cast<const int32_t*>(ws), parts);
 }
+
 
 }  // namespace kvc

@@ -231,9 +231,7 @@ int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64
     QuantJob jobs[2] = {
         {k_chunk, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
         {v_chunk, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
-    // one pass over HBM when the chunk fits the SMs' shared memory
-    e = launch_quant_fp4_fused(jobs, 2, n, c->dev_ws, attn_sm_count(), st);
-    if (e == cudaErrorNotSupported) e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
+    e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
   }
   if (e != cudaSuccess) return KVC_ECUDA;
   c->chunk_of_region[r] = chunk_idx;
@@ -375,13 +373,8 @@ int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream) {
   int32_t w = 0;
   if (cudaMemcpy(&w, c->dev_ws, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ECUDA;
   if (w != 0) {
-    // clear the error word and the encoder's grid-barrier counters (a wait
-    // that ran out can leave them mid-count)
-    const int32_t z[2] = {0, 0};
-    if (cudaMemcpy(c->dev_ws, z, sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(c->dev_ws + KVC_WS_WORDS - 2, z, 2 * sizeof(int32_t), cudaMemcpyHostToDevice) !=
-            cudaSuccess)
-      return KVC_ECUDA;
+    const int32_t z = 0;
+    if (cudaMemcpy(c->dev_ws, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return KVC_ECUDA;
     return KVC_ETIMEOUT;
   }
   return KVC_OK;
