@@ -310,7 +310,6 @@ __device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, 
 __global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, int64_t n,
                                                                const int32_t* __restrict__ ws,
                                                                int parts) {
-  __shared__ uint32_t red[32];
   __shared__ float gsh;
   __shared__ ScaleTab tab;
   const QuantJob job = blockIdx.y ? jobs.j[1] : jobs.j[0];
@@ -325,10 +324,16 @@ __global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, i
   int i = tid;
   load_pair(x, i, cnt, A);
   pdl_wait();  // the amax pass's partial maxima are complete and visible
-  uint32_t m = 0;
-  for (int k = tid; k < parts; k += kEncThreads) m = max(m, (uint32_t)__ldcg(ws + blockIdx.y * kQuantPartials + k));
-  m = block_max_u32(m, red);
-  if (tid == 0) gsh = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+  if (tid < 32) {  // one warp, all of its loads in flight at once
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kQuantPartials / 32; ++u) {
+      const int k = tid + 32 * u;
+      if (k < parts) m = max(m, (uint32_t)__ldcg(ws + blockIdx.y * kQuantPartials + k));
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (tid == 0) gsh = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+  }
   __syncthreads();
   const float g = gsh;
   if (blockIdx.x == 0 && tid == 0) *job.gscale = g;
