@@ -462,7 +462,7 @@ def main():
         rows[r] = d
     dom = max(("attn_bf16", "attn_fp4", "recache"), key=lambda r: per[r])
     kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>", "attn_fp4": "sinkwin_attn_kernel<128,true>",
-             "recache": "recache_kernel<256,4>"}[dom]
+             "recache": "recache_gemm_kernel<256,*> x2 + recache_norm_rope_kernel"}[dom]
     src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_attn.cu",
            "recache": "kernels_recache.cu"}[dom]
     tr = TRAFFIC.get(kname)
