@@ -338,10 +338,11 @@ def main():
     scale = 1.0 / math.sqrt(D)
     ROWS = ["recache", "evict_bf16", "append_bf16", "attn_bf16", "evict_fp4", "append_fp4", "attn_fp4"]
 
-    def step(L, evs=None):
+    def step(L, evs=None, wkv_t=None):
         c = L["c"] + 1
         present = [0] + list(range(c - W, c))
-        rec = (lambda: L["bf"].recache(L["hid"], wkv, gamma, present, GRID_H, GRID_W))
+        w = wkv if wkv_t is None else wkv_t
+        rec = (lambda: L["bf"].recache(L["hid"], w, gamma, present, GRID_H, GRID_W))
         ops = [rec,
                lambda: L["bf"].evict(c - W),
                lambda: L["bf"].append(L["k"], L["v"], c),
@@ -396,28 +397,61 @@ def main():
     ms_per_step = total_ms / args.steps
     value = STEP_FLOP * world / (ms_per_step * 1e-3) / 1e12
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step's
+    # inputs come from pinned host memory and its two attention outputs go back
+    # to it, all inside the timed region; the copies run on their own streams so
+    # that step s+1's inputs stream in (and step s-1's outputs stream out)
+    # while step s computes, and the host reads step s-1's result meanwhile.
     host = {n: layers[0][n].cpu().pin_memory() for n in ("q", "k", "v", "k4", "v4", "hid")}
     host["wkv"] = wkv.cpu().pin_memory()
-    out_h = [torch.empty((TC, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    out_h = [[torch.empty((TC, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+             for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_h)
+    d2h = sum(t.numel() * t.element_size() for t in out_h[0])
     n_e2e = max(3, min(args.steps, 10))
+    for L in layers:  # per-layer weight buffer: a copy never races a recache reading it
+        L["wkv"] = torch.empty_like(wkv)
+    comp = torch.cuda.current_stream()
+    cs, ds = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(n_e2e)]
+    done = [torch.cuda.Event() for _ in range(n_e2e)]
+    fetched = [torch.cuda.Event() for _ in range(n_e2e)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def enqueue_inputs(s):
+        L = layers[s % nlayers]
+        with torch.cuda.stream(cs):
+            if s >= nlayers:  # the layer's buffers are free once step s - nlayers is done
+                cs.wait_event(done[s - nlayers])
+            for n in ("q", "k", "v", "k4", "v4", "hid", "wkv"):
+                L[n].copy_(host[n], non_blocking=True)
+            copied[s].record(cs)
+
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e_start.record()
+    e_start.record(comp)
+    cs.wait_event(e_start)
+    enqueue_inputs(0)
     for s in range(n_e2e):
         L = layers[s % nlayers]
-        for n in ("q", "k", "v", "k4", "v4", "hid"):
-            L[n].copy_(host[n], non_blocking=True)
-        wkv.copy_(host["wkv"], non_blocking=True)
-        step(L)
-        out_h[0].copy_(L["o"], non_blocking=True)
-        out_h[1].copy_(L["o4"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()  # the host reads the step's result
-    e_end.record()
+        if s + 1 < n_e2e:
+            enqueue_inputs(s + 1)
+        comp.wait_event(copied[s])
+        if s >= nlayers:  # the layer's outputs of step s - nlayers have been read back
+            comp.wait_event(fetched[s - nlayers])
+        step(L, wkv_t=L["wkv"])
+        done[s].record(comp)
+        with torch.cuda.stream(ds):
+            ds.wait_event(done[s])
+            out_h[s % 2][0].copy_(L["o"], non_blocking=True)
+            out_h[s % 2][1].copy_(L["o4"], non_blocking=True)
+            fetched[s].record(ds)
+        if s >= 1:
+            fetched[s - 1].synchronize()  # the host reads step s-1's result
+    fetched[n_e2e - 1].synchronize()
+    comp.wait_event(fetched[n_e2e - 1])
+    e_end.record(comp)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end) / n_e2e
     if dist:
