@@ -61,6 +61,9 @@ def test_quant_bitexact_edge_values(swl):
     x = torch.from_numpy(np.concatenate(blocks)).to(torch.bfloat16)
     _check_quant(swl, x, "edge blocks")
     _check_quant(swl, torch.zeros(64, dtype=torch.bfloat16), "all zero")
+    # fewer 16-byte vectors than the amax pass has CTAs: one, two and 17 blocks
+    for nb in (1, 2, 17):
+        _check_quant(swl, x[: 16 * nb].clone(), f"{nb} block(s)")
     # many blocks: every CTA of both passes active, a grid-stride remainder
     y = torch.from_numpy(rng.standard_normal(16 * 300001).astype(np.float32)).to(torch.bfloat16)
     _check_quant(swl, y, "ragged size")
