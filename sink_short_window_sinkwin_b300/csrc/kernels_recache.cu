@@ -39,7 +39,7 @@ struct GemmParams {
   int32_t rows, HD, Tc;
   int32_t col0;    // first output column of this launch in [K | V]: 0 (K) or HD (V)
   int32_t ncol;    // column tiles (HD / BN)
-  int32_t ntiles;  // row tiles x column tiles
+  int32_t ntiles;  // tile groups: ceil(row tiles / cluster size) x column tiles
   int32_t region[kMaxSeg];
   __nv_bfloat16* k;
   __nv_bfloat16* v;
@@ -55,28 +55,47 @@ struct __align__(1024) GemmSmem {
   uint64_t bar_drain;
   uint32_t tmem_base;
   int32_t abort_flag;
+  // epilogue staging: per epilogue warp 32 rows x 32 words (+4 pad words per
+  // row, so both the row-wise writes and the transposed reads are conflict-free)
+  uint32_t stage[4][32][36];
 };
 
-// Persistent: CTA g takes tiles g, g + G, ... (row-major over [row tile][column
-// tile], so consecutive tiles of a CTA share hidden rows through L2).  The
-// accumulator alternates between two TMEM buffers, so the epilogue of one tile
-// overlaps the MMAs of the next.
+// Persistent, in clusters of kC CTAs.  A tile group is kC consecutive row tiles
+// x one column tile; cluster c takes groups c, c + NC, ... (row-major over
+// [row group][column tile], so consecutive groups share hidden rows through
+// L2) and its CTA of rank r computes row tile (group row) * kC + r.  The kC
+// CTAs of a group need the same B tile: each loads its own A tile and a 1/kC
+// share of B, multicast into every CTA of the cluster, which cuts the L2 -> SM
+// operand traffic per tile by a third (kC = 2) or a half (kC = 4).  A ring
+// stage is refilled only once the MMAs of all kC CTAs have consumed it, so its
+// empty barrier counts kC commits (each CTA commits to all of them).  Row tiles
+// past the last row load as TMA zero fill and store nothing.  The accumulator
+// alternates between two TMEM buffers, so the epilogue of one tile overlaps the
+// MMAs of the next.
 // kKf32: K launch (fp32 rows parked in the K|V rows); else the V launch (bf16).
-template <int BN, bool kKf32>
+template <int BN, bool kKf32, int kC>
 __global__ void __launch_bounds__(kRThreads, 1)
     recache_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
+  static_assert(kC == 1 || kC == 2 || kC == 4, "cluster size");
+  static_assert((BN / 64) % kC == 0, "each CTA loads whole 64-column boxes of B");
   using Smem = GemmSmem<BN>;
   constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
+  constexpr uint16_t kMask = (uint16_t)((1u << kC) - 1u);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.HD / RK;
+  const int rank = kC > 1 ? (int)cluster_ctarank() : 0;
+  const int cid = blockIdx.x / kC, ncl = gridDim.x / kC;  // cluster index, clusters
+  // row tile and first column of tile group t for this CTA
+  auto tile_m0 = [&](int t) { return ((t / p.ncol) * kC + rank) * RM; };
+  auto tile_n0 = [&](int t) { return (t % p.ncol) * BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.bar_full[s], 1);
-      mbar_init(&sm.bar_empty[s], 1);
+      mbar_init(&sm.bar_empty[s], kC);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.bar_acc_full[b], 1);
@@ -92,6 +111,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // the other CTAs' multicast copies and commits target this CTA's barriers:
+  // every CTA of the cluster initialises its barriers before any is used
+  if constexpr (kC > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const Watchdog wd{&sm.abort_flag, p.dev_err};
@@ -102,24 +124,41 @@ __global__ void __launch_bounds__(kRThreads, 1)
       tma_prefetch_desc(&tmB);
       int issued = 0;  // K-steps loaded by this CTA (ring position)
       bool ok = true;
-      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
-        const int m0 = (t / p.ncol) * RM, nloc = (t % p.ncol) * BN;
+      for (int t = cid; t < p.ntiles && ok; t += ncl) {
+        const int m0 = tile_m0(t), nloc = tile_n0(t);
         for (int kb = 0; kb < nk; ++kb, ++issued) {
           const int s = issued % kStages, u = issued / kStages;
           if (issued >= kStages && !mbar_wait(&sm.bar_empty[s], (u - 1) & 1, wd)) {
             ok = false;
             break;
           }
+          // this CTA's A tile plus the whole B tile (its own share and the
+          // shares the other CTAs of the cluster multicast here)
           mbar_expect_tx(&sm.bar_full[s], RM * RK * 2 + RK * BN * 2);
           tma_load_2d(&sm.a[s][0], &tmA, &sm.bar_full[s], kb * RK, m0);
-          for (int nb = 0; nb < BN / 64; ++nb)
-            tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
+          constexpr int kBoxes = BN / 64 / kC;  // B boxes this CTA loads
+#pragma unroll
+          for (int q = 0; q < kBoxes; ++q) {
+            const int nb = rank * kBoxes + q;
+            if constexpr (kC > 1)
+              tma_load_2d_mc(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK, kMask);
+            else
+              tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
+          }
         }
       }
       if (sm.abort_flag) {  // every copy this thread started lands before the CTA exits
         for (int s = 0; s < kStages; ++s) {
           const int cnt = issued > s ? (issued - s + kStages - 1) / kStages : 0;
           if (cnt) mbar_drain(&sm.bar_full[s], (cnt - 1) & 1);
+        }
+      }
+      if constexpr (kC > 1) {
+        // the last commits of every stage (from all kC CTAs, some remote) have
+        // arrived before this CTA's shared memory goes away
+        for (int s = 0; s < kStages; ++s) {
+          const int cnt = issued > s ? (issued - s + kStages - 1) / kStages : 0;
+          if (cnt) mbar_drain(&sm.bar_empty[s], (cnt - 1) & 1);
         }
       }
     }
@@ -129,7 +168,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       int used = 0;  // K-steps consumed (ring position)
       int j = 0;     // tiles of this CTA
       bool ok = true;
-      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++j) {
+      for (int t = cid; t < p.ntiles && ok; t += ncl, ++j) {
         const int buf = j & 1;
         if (j >= 2 && !mbar_wait(&sm.bar_acc_empty[buf], ((j >> 1) - 1) & 1, wd)) break;
         tc_fence_after();
@@ -147,7 +186,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
             const uint64_t bd = sdesc_sw128(smem_u32(&sm.b[s][0][0]) + kk * 2048, RK * 128, 1024);
             mma_bf16_ss(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&sm.bar_empty[s]);
+          if constexpr (kC > 1)
+            mma_commit_mc(&sm.bar_empty[s], kMask);  // frees the stage in every CTA of the cluster
+          else
+            mma_commit(&sm.bar_empty[s]);
         }
         if (ok) mma_commit(&sm.bar_acc_full[buf]);
       }
@@ -156,43 +198,64 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
+    const int wq = warp & 3;  // TMEM lane quarter: rows 32 wq .. 32 wq + 31 of the tile
     int j = 0;
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++j) {
+    for (int t = cid; t < p.ntiles; t += ncl, ++j) {
       const int buf = j & 1;
-      const int m0 = (t / p.ncol) * RM, nloc = (t % p.ncol) * BN;
+      const int m0 = tile_m0(t), nloc = tile_n0(t);
       const uint32_t trow = tmem + (uint32_t)(buf * BN) + ((uint32_t)(wq * 32) << 16);
       // tcgen05.ld is warp-collective (.sync.aligned): the whole warp loads, and
       // only the stores are predicated on the row being real (the last row tile
       // can end inside a warp)
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_acc_full[buf], (j >> 1) & 1, wd))) break;
       tc_fence_after();
-      const int grow = m0 + r;
-      const bool live = grow < p.rows;
-      const int ci = live ? grow / p.Tc : 0;
-      const int64_t dest = (int64_t)p.region[ci] * p.Tc + (grow - ci * p.Tc);
+      // Each 32-column chunk goes through the warp's staging rows (lane = row)
+      // and back out transposed: in store step k, lane l writes one 16-byte
+      // piece of row k * (32 / pieces) + l / pieces, so each store instruction
+      // covers whole 128-byte (fp32) or 64-byte (bf16) row segments instead of
+      // 16 bytes of 32 different rows.
+      uint32_t (*stg)[36] = sm.stage[wq];
 #pragma unroll 1
       for (int jj = 0; jj < BN / 32; ++jj) {
         uint32_t x[32];
         tmem_ld32(trow + jj * 32, x);
         tmem_ld_wait();
-        if (!live) continue;
         const int col = nloc + jj * 32;  // column within the half, a multiple of 32
+        __syncwarp();                    // the previous chunk's transposed reads are done
         if constexpr (kKf32) {
-          const int half = p.HD / 2;
-          float* row = reinterpret_cast<float*>(col < half ? p.k + dest * p.HD : p.v + dest * p.HD);
-          uint4* d4 = reinterpret_cast<uint4*>(row + (col < half ? col : col - half));
+          // fp32: 32 words per row
 #pragma unroll
-          for (int e = 0; e < 8; ++e) d4[e] = make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(&stg[lane][4 * e]) = make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
         } else {
-          uint4* d4 = reinterpret_cast<uint4*>(p.v + dest * p.HD + col);
+          // bf16: 16 words per row
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            d4[e] = make_uint4(pack_bf16x2(__uint_as_float(x[8 * e + 0]), __uint_as_float(x[8 * e + 1])),
-                               pack_bf16x2(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3])),
-                               pack_bf16x2(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5])),
-                               pack_bf16x2(__uint_as_float(x[8 * e + 6]), __uint_as_float(x[8 * e + 7])));
+            *reinterpret_cast<uint4*>(&stg[lane][4 * e]) =
+                make_uint4(pack_bf16x2(__uint_as_float(x[8 * e + 0]), __uint_as_float(x[8 * e + 1])),
+                           pack_bf16x2(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3])),
+                           pack_bf16x2(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5])),
+                           pack_bf16x2(__uint_as_float(x[8 * e + 6]), __uint_as_float(x[8 * e + 7])));
+        }
+        __syncwarp();
+        constexpr int kChunksPerRow = kKf32 ? 8 : 4;  // 16-byte pieces of a row's 32 values
+        constexpr int kRowsPerStep = 32 / kChunksPerRow;
+#pragma unroll
+        for (int k = 0; k < 32 / kRowsPerStep; ++k) {
+          const int rl = k * kRowsPerStep + lane / kChunksPerRow;  // row within the warp's 32
+          const int piece = lane % kChunksPerRow;
+          const int gr = m0 + wq * 32 + rl;
+          if (gr >= p.rows) continue;
+          const int ci = gr / p.Tc;
+          const int64_t dst = (int64_t)p.region[ci] * p.Tc + (gr - ci * p.Tc);
+          const uint4 v = *reinterpret_cast<const uint4*>(&stg[rl][4 * piece]);
+          if constexpr (kKf32) {
+            const int half = p.HD / 2;
+            float* row = reinterpret_cast<float*>(col < half ? p.k + dst * p.HD : p.v + dst * p.HD);
+            reinterpret_cast<uint4*>(row + (col < half ? col : col - half))[piece] = v;
+          } else {
+            reinterpret_cast<uint4*>(p.v + dst * p.HD + col)[piece] = v;
+          }
         }
       }
       tc_fence_before();
@@ -295,21 +358,91 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
   }
 }
 
-template <int BN, bool kKf32>
-cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
-                        cudaStream_t st) {
+// Whole clusters that can be resident at once for a kC-CTA cluster launch of
+// this kernel (0 if none).
+template <int BN, bool kKf32, int kC>
+int clusters_that_fit() {
+  static int cache[64] = {};  // per device; -1: queried, none fit
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev]) return cache[dev] > 0 ? cache[dev] : 0;
+  auto kern = recache_gemm_kernel<BN, kKf32, kC>;
   const size_t smem = sizeof(GemmSmem<BN>) + 1024;
-  auto kern = recache_gemm_kernel<BN, kKf32>;
+  static bool smem_set[64] = {};
+  int fit = 0;
+  if (set_smem_once(kern, smem, smem_set) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(attn_sm_count() / kC * kC), 1, 1);
+    cfg.blockDim = dim3(kRThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) fit = 0;
+  }
+  (void)cudaGetLastError();
+  cache[dev] = fit > 0 ? fit : -1;
+  return fit;
+}
+
+template <int BN, bool kKf32, int kC>
+cudaError_t launch_gemm_c(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
+                          cudaStream_t st) {
+  const size_t smem = sizeof(GemmSmem<BN>) + 1024;
+  auto kern = recache_gemm_kernel<BN, kKf32, kC>;
   static bool smem_set[64] = {};  // one per instantiation of this launcher
   cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
-  p.ncol = p.HD / BN;
-  p.ntiles = ((rows + RM - 1) / RM) * p.ncol;
-  int nsm = attn_sm_count();
+  const int nsm = attn_sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
-  const int grid = p.ntiles < nsm ? p.ntiles : nsm;
-  kern<<<grid, kRThreads, smem, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  p.ncol = p.HD / BN;
+  const int row_tiles = (rows + RM - 1) / RM;
+  p.ntiles = ((row_tiles + kC - 1) / kC) * p.ncol;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kRThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // one CTA per SM, as many whole clusters as fit at once (persistent)
+  int clusters = nsm / kC;
+  if constexpr (kC > 1) {
+    const int fit = clusters_that_fit<BN, kKf32, kC>();
+    if (fit < 1) return cudaErrorNotSupported;
+    clusters = fit < clusters ? fit : clusters;
+  }
+  if (clusters > p.ntiles) clusters = p.ntiles;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(clusters * kC, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+}
+
+// B is shared by clusters of 4 (or 2) CTAs, whole 64-column boxes each, when
+// such clusters still cover (nearly) every SM; otherwise the plain kernel.  On
+// a GPU whose SMs do not split evenly into clusters the larger cluster can
+// leave SMs idle, which costs more than the shared B saves.
+template <int BN, bool kKf32>
+cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
+                        cudaStream_t st) {
+  const int nsm = attn_sm_count();
+  if constexpr (BN / 64 >= 4) {
+    if (clusters_that_fit<BN, kKf32, 4>() * 4 >= nsm - 2)
+      return launch_gemm_c<BN, kKf32, 4>(rows, ta, tb, p, st);
+  }
+  if constexpr (BN / 64 >= 2) {
+    if (clusters_that_fit<BN, kKf32, 2>() * 2 >= nsm - 2)
+      return launch_gemm_c<BN, kKf32, 2>(rows, ta, tb, p, st);
+  }
+  return launch_gemm_c<BN, kKf32, 1>(rows, ta, tb, p, st);
 }
 
 template <int BN, int HD>
