@@ -143,7 +143,8 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
  *   [K | V] = hidden @ w_kv;  K <- RoPE3D(RMSNorm(K) * gamma_k);  written to the
  *   chunks' regions.
  * hidden: device bf16 [n*Tc][H*D]; w_kv: device bf16 [H*D][2*H*D], the K columns
- * first; gamma_k: device fp32 [H*D] or NULL (= ones).  RMSNorm spans the whole
+ * first; gamma_k: device fp32 [H*D], 16-byte aligned, or NULL (= ones); hidden and
+ * w_kv 16-byte aligned (else KVC_EINVAL).  RMSNorm spans the whole
  * H*D-wide K row: x / sqrt(mean(x^2) + eps).  3D RoPE: token t of chunk c is at
  * frame c*chunk_frames + t / tokens_per_frame, row (t % tpf) / grid_w, column
  * t % grid_w (grid_h * grid_w == tokens_per_frame); the D/2 rotation pairs

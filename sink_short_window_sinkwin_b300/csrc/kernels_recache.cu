@@ -215,10 +215,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
       // covers whole 128-byte (fp32) or 64-byte (bf16) row segments instead of
       // 16 bytes of 32 different rows.
       uint32_t (*stg)[36] = sm.stage[wq];
+      // The TMEM load of chunk jj + 1 is in flight while chunk jj is stored.
+      uint32_t x[32];
+      tmem_ld32(trow, x);
 #pragma unroll 1
       for (int jj = 0; jj < BN / 32; ++jj) {
-        uint32_t x[32];
-        tmem_ld32(trow + jj * 32, x);
         tmem_ld_wait();
         const int col = nloc + jj * 32;  // column within the half, a multiple of 32
         __syncwarp();                    // the previous chunk's transposed reads are done
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                            pack_bf16x2(__uint_as_float(x[8 * e + 6]), __uint_as_float(x[8 * e + 7])));
         }
         __syncwarp();
+        if (jj + 1 < BN / 32) tmem_ld32(trow + (jj + 1) * 32, x);  // x is free again
         constexpr int kChunksPerRow = kKf32 ? 8 : 4;  // 16-byte pieces of a row's 32 values
         constexpr int kRowsPerStep = 32 / kChunksPerRow;
 #pragma unroll
@@ -344,14 +346,13 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
       pr_cached = pr0;
     }
     const float v4[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+    const float4 g4 = p.gamma ? __ldg(reinterpret_cast<const float4*>(p.gamma) + c4) : make_float4(1.f, 1.f, 1.f, 1.f);
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
     uint32_t o[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int c = col + 2 * e;
-      const float g0 = p.gamma ? p.gamma[c] : 1.0f;
-      const float g1 = p.gamma ? p.gamma[c + 1] : 1.0f;
-      const float y0 = v4[2 * e] * rstd * g0;
-      const float y1 = v4[2 * e + 1] * rstd * g1;
+      const float y0 = v4[2 * e] * rstd * gv[2 * e];
+      const float y1 = v4[2 * e + 1] * rstd * gv[2 * e + 1];
       o[e] = pack_bf16x2(y0 * cs[e] - y1 * sn[e], y0 * sn[e] + y1 * cs[e]);
     }
     out[c4] = make_uint2(o[0], o[1]);

@@ -319,7 +319,7 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
                     float rope_theta, kvc_stream_t stream) {
   if (!ready(c) || !hidden || !w_kv || !chunk_ids || n < 1 || n > 1 + c->window_chunks)
     return KVC_EINVAL;
-  if (!aligned16(hidden) || !aligned16(w_kv) || (gamma_k && (reinterpret_cast<uintptr_t>(gamma_k) & 3u)))
+  if (!aligned16(hidden) || !aligned16(w_kv) || (gamma_k && !aligned16(gamma_k)))
     return KVC_EINVAL;
   if (grid_h < 1 || grid_w < 1 || (int64_t)grid_h * grid_w != c->tokens_per_frame) return KVC_EINVAL;
   if (!(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta > 0.0f) || !std::isfinite(rope_theta))

@@ -117,6 +117,11 @@ def test_recache_rejections(swl):
     with pytest.raises(swl.KvcError) as e:
         cache.recache(hid.cuda(), wkv.cuda(), None, [0, 2, 1], sh.grid_h, sh.grid_w)
     assert e.value.status == swl.KVC_ESTATE
+    # gamma must be 16-byte aligned (read as float4): a view one float in is refused
+    g_off = torch.ones(sh.heads * sh.head_dim + 1, dtype=torch.float32, device="cuda")[1:]
+    with pytest.raises(swl.KvcError) as e:
+        cache.recache(hid.cuda(), wkv.cuda(), g_off, [0, 1, 2], sh.grid_h, sh.grid_w)
+    assert e.value.status == swl.KVC_EINVAL
     f = swl.KVCache(1, 64, 16, 2, 2, dtype="fp4")
     z = torch.zeros((32, 1, 64), dtype=torch.bfloat16, device="cuda")
     f.append(z, z, 0)
