@@ -66,7 +66,7 @@ struct __align__(1024) GemmSmem {
 // L2) and its CTA of rank r computes row tile (group row) * kC + r.  The kC
 // CTAs of a group need the same B tile: each loads its own A tile and a 1/kC
 // share of B, multicast into every CTA of the cluster, which cuts the L2 -> SM
-// operand traffic per tile by a third (kC = 2) or a half (kC = 4).  A ring
+// operand traffic per tile by a third (kC = 2).  A ring
 // stage is refilled only once the MMAs of all kC CTAs have consumed it, so its
 // empty barrier counts kC commits (each CTA commits to all of them).  Row tiles
 // past the last row load as TMA zero fill and store nothing.  The accumulator
@@ -77,7 +77,7 @@ template <int BN, bool kKf32, int kC>
 __global__ void __launch_bounds__(kRThreads, 1)
     recache_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
-  static_assert(kC == 1 || kC == 2 || kC == 4, "cluster size");
+  static_assert(kC == 1 || kC == 2, "cluster size");
   static_assert((BN / 64) % kC == 0, "each CTA loads whole 64-column boxes of B");
   using Smem = GemmSmem<BN>;
   constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
@@ -427,18 +427,15 @@ cudaError_t launch_gemm_c(int rows, const CUtensorMap& ta, const CUtensorMap& tb
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
-// B is shared by clusters of 4 (or 2) CTAs, whole 64-column boxes each, when
-// such clusters still cover (nearly) every SM; otherwise the plain kernel.  On
-// a GPU whose SMs do not split evenly into clusters the larger cluster can
-// leave SMs idle, which costs more than the shared B saves.
+// B is shared by clusters of 2 CTAs (whole 64-column boxes each) when such
+// clusters still cover (nearly) every SM; otherwise the plain kernel.  Clusters
+// of 4 would halve the B traffic rather than cut it by a third, but on a B300
+// only 33 of them (132 SMs) can be resident at once, which costs more than the
+// shared B saves.
 template <int BN, bool kKf32>
 cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
                         cudaStream_t st) {
   const int nsm = attn_sm_count();
-  if constexpr (BN / 64 >= 4) {
-    if (clusters_that_fit<BN, kKf32, 4>() * 4 >= nsm - 2)
-      return launch_gemm_c<BN, kKf32, 4>(rows, ta, tb, p, st);
-  }
   if constexpr (BN / 64 >= 2) {
     if (clusters_that_fit<BN, kKf32, 2>() * 2 >= nsm - 2)
       return launch_gemm_c<BN, kKf32, 2>(rows, ta, tb, p, st);

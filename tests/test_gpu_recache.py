@@ -91,6 +91,19 @@ def test_recache_two_column_tiles_noncontiguous_positions(swl):
     _compare_cache(cache, model, sh, what="two tiles")
 
 
+@pytest.mark.parametrize("heads,head_dim", [(1, 128), (2, 128), (6, 128)])
+def test_recache_cluster_tile_widths(swl, heads, head_dim):
+    """H*D = 128, 256, 768: GEMM column tiles 128 or 256 wide (one, one and three
+    of them), the B tile shared by a 2-CTA cluster.  Three 120-token chunks are
+    three row tiles, so one CTA of the second cluster computes a row tile past
+    the last row (loaded as zeros, nothing stored)."""
+    sh = Shapes(heads, head_dim, 40, 3, 2, 4, 10)
+    cache, model = _fill(swl, sh, 2)
+    assert model.present_chunks() == [0, 1, 2]
+    _recache_both(swl, sh, cache, model, 7, gamma_rand=True)
+    _compare_cache(cache, model, sh, what=f"H*D={heads * head_dim}")
+
+
 def test_recache_layer_full_size_then_attention(swl):
     """Prompt switch before chunk 4: chunks {0,1,2,3} = 12 frames, 18720 x 1536
     hidden states, then one 4680-query attention step over the rebuilt cache."""
