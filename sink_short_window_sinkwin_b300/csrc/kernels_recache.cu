@@ -46,6 +46,13 @@ struct GemmParams {
   int32_t* dev_err;
 };
 
+// Slot of 16-byte piece c of staged row r: c ^ f(r) with f(r) = 4 (r & 1) +
+// (r >> 1) % 4, a permutation of 0..7 over any 8 consecutive rows, and with bit
+// 2 different for the two rows of an even/odd pair.  So 8 lanes writing piece c
+// of 8 consecutive rows, 8 lanes reading pieces 0..7 of one row, and 4 + 4 lanes
+// reading pieces 0..3 of rows 2i and 2i+1 each touch 8 different bank groups.
+__device__ __forceinline__ int stage_slot(int r, int c) { return c ^ (((r & 1) << 2) | ((r >> 1) & 3)); }
+
 template <int BN>
 struct __align__(1024) GemmSmem {
   __nv_bfloat16 a[kStages][RM * RK];
@@ -55,9 +62,10 @@ struct __align__(1024) GemmSmem {
   uint64_t bar_drain;
   uint32_t tmem_base;
   int32_t abort_flag;
-  // epilogue staging: per epilogue warp 32 rows x 32 words (+4 pad words per
-  // row, so both the row-wise writes and the transposed reads are conflict-free)
-  uint32_t stage[4][32][36];
+  // epilogue staging: per epilogue warp 32 rows x 32 words, 16-byte pieces
+  // placed by stage_slot() so that the row-wise writes and the transposed reads
+  // are both free of bank conflicts
+  uint32_t stage[4][32][32];
 };
 
 // Persistent, in clusters of kC CTAs.  A tile group is kC consecutive row tiles
@@ -214,7 +222,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
       // piece of row k * (32 / pieces) + l / pieces, so each store instruction
       // covers whole 128-byte (fp32) or 64-byte (bf16) row segments instead of
       // 16 bytes of 32 different rows.
-      uint32_t (*stg)[36] = sm.stage[wq];
+      uint32_t (*stg)[32] = sm.stage[wq];
+      // cache row of this lane's tile row (lane = row within the warp's 32);
+      // store steps fetch the row they write from its lane
+      int64_t my_dest = 0;
+      {
+        const int gr = m0 + wq * 32 + lane;
+        if (gr < p.rows) {
+          const int ci = gr / p.Tc;
+          my_dest = (int64_t)p.region[ci] * p.Tc + (gr - ci * p.Tc);
+        }
+      }
       // The TMEM load of chunk jj + 1 is in flight while chunk jj is stored.
       uint32_t x[32];
       tmem_ld32(trow, x);
@@ -227,12 +245,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
           // fp32: 32 words per row
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint4*>(&stg[lane][4 * e]) = make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+            *reinterpret_cast<uint4*>(&stg[lane][4 * stage_slot(lane, e)]) =
+                make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
         } else {
           // bf16: 16 words per row
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(&stg[lane][4 * e]) =
+            *reinterpret_cast<uint4*>(&stg[lane][4 * stage_slot(lane, e)]) =
                 make_uint4(pack_bf16x2(__uint_as_float(x[8 * e + 0]), __uint_as_float(x[8 * e + 1])),
                            pack_bf16x2(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3])),
                            pack_bf16x2(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5])),
@@ -246,11 +265,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
         for (int k = 0; k < 32 / kRowsPerStep; ++k) {
           const int rl = k * kRowsPerStep + lane / kChunksPerRow;  // row within the warp's 32
           const int piece = lane % kChunksPerRow;
-          const int gr = m0 + wq * 32 + rl;
-          if (gr >= p.rows) continue;
-          const int ci = gr / p.Tc;
-          const int64_t dst = (int64_t)p.region[ci] * p.Tc + (gr - ci * p.Tc);
-          const uint4 v = *reinterpret_cast<const uint4*>(&stg[rl][4 * piece]);
+          const int64_t dst = __shfl_sync(0xffffffffu, my_dest, rl);
+          if (m0 + wq * 32 + rl >= p.rows) continue;
+          const uint4 v = *reinterpret_cast<const uint4*>(&stg[rl][4 * stage_slot(rl, piece)]);
           if constexpr (kKf32) {
             const int half = p.HD / 2;
             float* row = reinterpret_cast<float*>(col < half ? p.k + dst * p.HD : p.v + dst * p.HD);
