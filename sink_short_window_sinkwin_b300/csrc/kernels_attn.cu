@@ -73,6 +73,7 @@ struct AttnParams {
   const float* kg;
   const float* vg;
   int32_t Tc;
+  int32_t seg_region[kMaxSeg];  // region of each segment (an FP4 segment lies in one)
 };
 
 template <int D>
@@ -649,7 +650,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           // two passes over 32-column chunks (fewer live registers).  The tile
           // lies in one region: its K tensor scale joins the logit scale, its
           // V tensor scale multiplies P (stored as f16 for the f16 P*V MMA)
-          const int region = p.seg[cur.seg].row0 / p.Tc;
+          const int region = p.seg_region[cur.seg];
           const float cg = c * p.kg[region];
           const float gv = p.vg[region];
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -877,6 +878,7 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   p.kg = a.k_gscale;
   p.vg = a.v_gscale;
   p.Tc = a.chunk_tokens;
+  for (int i = 0; i < a.nseg; ++i) p.seg_region[i] = p.Tc > 0 ? a.seg[i].row0 / p.Tc : 0;
   // schedule: at most one CTA per SM and per item, so every item spans at
   // most two neighbouring shares
   const int nsm = sm_count();
