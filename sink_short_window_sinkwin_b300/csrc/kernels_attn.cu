@@ -535,6 +535,8 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     uint32_t it = 0;
     int ns = 0, no = 0;
     bool ok = true;
+    int kv_region = -1;  // FP4: region whose tensor scales are held below
+    float kv_kg = 0.0f, kv_vg = 0.0f;
     while (ok && sh.next(p, pc)) {
       const int h = pc.u / p.n_pairs;
       const int m0 = (pc.u % p.n_pairs) * (2 * BM);
@@ -651,8 +653,13 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           // lies in one region: its K tensor scale joins the logit scale, its
           // V tensor scale multiplies P (stored as f16 for the f16 P*V MMA)
           const int region = p.seg_region[cur.seg];
-          const float cg = c * p.kg[region];
-          const float gv = p.vg[region];
+          if (region != kv_region) {  // consecutive tiles mostly share a region
+            kv_region = region;
+            kv_kg = __ldg(p.kg + region);
+            kv_vg = __ldg(p.vg + region);
+          }
+          const float cg = c * kv_kg;
+          const float gv = kv_vg;
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
           for (int j = 0; j < BN / 32; ++j) {
