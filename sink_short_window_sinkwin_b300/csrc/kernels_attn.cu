@@ -166,10 +166,12 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t word, uint32_t (&d)[4])
       : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
       : "r"(word));
 }
-__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
-  if (e == 0) return (float)m * 0.001953125f;
-  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+// two E4M3 block scales (low byte first) -> f16x2 (exact: E4M3 values lie in
+// the f16 normal range)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(two_bytes));
+  return d;
 }
 
 // One key row of FP4 codes and block scales, held in registers so the loads
@@ -216,11 +218,12 @@ __device__ __forceinline__ void decode_row(__nv_bfloat16 (*dst)[BN * 64], int r,
 #pragma unroll
   for (int q16 = 0; q16 < D / 32; ++q16) {  // 16 code bytes = 32 elements = 2 blocks
     const uint32_t w[4] = {raw.c[q16].x, raw.c[q16].y, raw.c[q16].z, raw.c[q16].w};
+    // the scales of blocks 2 q16 and 2 q16 + 1 (bytes 2 q16, 2 q16 + 1 of the row's scales)
+    const uint32_t spair = e4m3x2_to_f16x2(raw.s[q16 >> 1] >> (16 * (q16 & 1)));
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // one 16-element block -> two 16-byte chunks
-      const int b = q16 * 2 + half;
-      const uint32_t sc = (raw.s[b >> 2] >> (8 * (b & 3))) & 0xFFu;
-      const __half2 s2 = __float2half2_rn(e4m3_to_f32(sc));  // exact
+      const __half2 sp = *reinterpret_cast<const __half2*>(&spair);
+      const __half2 s2 = half ? __high2half2(sp) : __low2half2(sp);
       uint32_t outw[8];
 #pragma unroll
       for (int wi = 0; wi < 2; ++wi) {
