@@ -121,6 +121,43 @@ def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
                  plus_output_rounding=True)
 
 
+@pytest.mark.parametrize("where", ["every_tile", "late_tile"])
+def test_fp4_max_jump_within_tile(swl, where):
+    """Keys 64..127 of a 128-key tile whose logits lie more than 2^8 (log2
+    units) above those of keys 0..63: the softmax moves its reference in the
+    middle of the tile and rescales the P it already wrote for the first half.
+    256-token chunks = two tiles each; queries 10u + noise, planted keys 10u
+    (u a unit vector).  every_tile: the jump comes on each piece's first tile;
+    late_tile: only the last tile of chunk 2 has it, after other tiles set the
+    reference."""
+    H, D, Tc, W = 2, 128, 256, 2
+    rng = np.random.default_rng(31)
+    u = rng.standard_normal(D)
+    u /= np.linalg.norm(u)
+    cache = swl.KVCache(H, D, 128, 2, W, dtype="fp4")
+    model = CacheModel(H, D, Tc, W)
+    for c in range(1 + W):
+        k = rng.standard_normal((Tc, H, D)) * 0.3
+        v = rng.standard_normal((Tc, H, D))
+        if where == "every_tile":
+            k[64:128] = 10 * u
+            k[192:256] = 10 * u
+        elif c == W:
+            k[192:256] = 10 * u
+        kb = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16)
+        vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+        cache.append(kb.cuda(), vb.cuda(), c)
+        model.append(c, ofp4.dequantize(*ofp4.quantize(_f32(kb))), ofp4.dequantize(*ofp4.quantize(_f32(vb))))
+    q = 10 * u + 0.3 * rng.standard_normal((130, H, D))
+    qb = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    out = cache.attn(qb.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(qb), scale)
+    assert_close(to64(out), want, ATOL_FP4, None, f"fp4 max jump ({where})", plus_output_rounding=True)
+    assert cache.last_device_error() == swl.KVC_OK
+
+
 def test_fp4_layer_full_size(swl):
     sh = LAYER_1P3B
     scale = 1.0 / math.sqrt(sh.head_dim)
