@@ -14,6 +14,8 @@ from .inputs import (  # noqa: F401
     gaussian_bf16,
     gaussian_outliers_bf16,
     chunk_qkv,
+    chunk_qkv_device,
+    device_seed,
     recache_inputs,
     bf16_to_f64,
 )

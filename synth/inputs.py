@@ -116,6 +116,35 @@ def chunk_qkv(sh: Shapes, cfg: int, layer: int, chunk: int, dist: str = "rms1",
     return q, k, v
 
 
+def device_seed(*parts: int) -> int:
+    """63-bit seed for torch's device generator, derived from a seed tuple."""
+    w = np.random.SeedSequence([int(p) for p in parts]).generate_state(2, np.uint32)
+    return (int(w[0]) << 31) ^ int(w[1])
+
+
+def chunk_qkv_device(sh: Shapes, cfg: int, layer: int, chunk: int, device="cuda"):
+    """Q, K, V of one chunk drawn on the GPU, bf16 [Tc][H][D] each, with the
+    single-layer distribution: Q, K elementwise N(0,1)/sqrt(D), V N(0,1).
+
+    Each tensor comes from torch's counter-based device generator seeded by
+    (config, layer, chunk, tensor id), drawn in float32 and rounded once to
+    bfloat16, so re-drawing the same key reproduces it bit for bit: a test can
+    rebuild any past chunk for the oracle instead of keeping it.  Used where
+    the stream is too long to draw on the host (hundreds of chunks x layers).
+    """
+    shp = (sh.chunk_tokens, sh.heads, sh.head_dim)
+    s = float(np.float32(1.0 / np.sqrt(sh.head_dim)))
+    out = []
+    for tid, std in ((_TID_Q, s), (_TID_K, s), (_TID_V, 1.0)):
+        g = torch.Generator(device=device)
+        g.manual_seed(device_seed(cfg, layer, chunk, tid))
+        a = torch.randn(shp, generator=g, device=device, dtype=torch.float32)
+        if std != 1.0:
+            a.mul_(std)
+        out.append(a.to(torch.bfloat16))
+    return tuple(out)
+
+
 def recache_inputs(sh: Shapes, cfg: int, n_chunks: int, w_std: float = 0.02):
     """Hidden states [n*Tc][H*D] ~ N(0,1), K|V weight [H*D][2*H*D] ~ N(0, w_std^2),
     RMSNorm gain (all ones, float32)."""

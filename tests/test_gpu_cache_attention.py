@@ -10,7 +10,7 @@ import torch
 
 from oracle import attention as oatt
 from oracle.cache_model import CacheModel, CacheStateError
-from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, bf16_to_f64
+from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, chunk_qkv_device, bf16_to_f64
 from tests.gpu_helpers import (ATOL_BF16, RELL2_BF16, SAMPLE_ROWS_4680, assert_close, to64)
 
 pytestmark = pytest.mark.gpu
@@ -190,6 +190,65 @@ def test_append_copy_is_exact_full_size(swl):
         _, k, v = chunk_qkv(sh, 1, 0, c, "literal")
         sl = slice(c * sh.chunk_tokens, (c + 1) * sh.chunk_tokens)
         assert torch.equal(cache.k[sl].cpu(), k) and torch.equal(cache.v[sl].cpu(), v)
+
+
+def test_rolling_stream_30_layers_320_chunks(swl):
+    """Rolling stream: 30 independent layer caches x 320 chunks (960 latent
+    frames), each step evict(c - W) + append(c) + attention, the sink pinned;
+    Q/K/V are drawn per (layer, chunk) on the device.  Every step checks the
+    slot map against the oracle model.  Sampled (layer, chunk) steps -- the
+    warm-up, the first eviction, mid-stream, the last chunk -- check sampled
+    query rows against the float64 oracle over the visible chunks re-drawn
+    from their seeds.  At the end every layer holds exactly chunks 0, 317, 318
+    and 319, bit for bit.  Prints the steady-state (c >= 4) latent frames/s
+    per layer, from CUDA events around each layer's evict + append + attention."""
+    sh = LAYER_1P3B
+    cfg, n_layers, n_chunks, W = 2, 30, 320, sh.window_chunks
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    rows = [0, 127, 128, 1560, 3119, 4095, 4608, 4679]
+    checks = {(0, 0), (1, 1), (2, 2), (3, 3), (4, 4), (29, 5), (17, 100), (5, 201), (0, 319), (29, 319)}
+    caches = [swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, W)
+              for _ in range(n_layers)]
+    slot_maps = [CacheModel(1, 1, 1, W) for _ in range(n_layers)]  # slot rule only
+    z1 = np.zeros((1, 1, 1))
+    steady = []
+    for c in range(n_chunks):
+        for li in range(n_layers):
+            q, k, v = chunk_qkv_device(sh, cfg, li, c)
+            cache, model = caches[li], slot_maps[li]
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            if c > W:
+                cache.evict(c - W)
+                model.evict(c - W)
+            cache.append(k, v, c)
+            model.append(c, z1, z1)
+            out = cache.attn(q, scale)
+            t1.record()
+            assert cache.chunk_of_region == model.chunk_of_region, (li, c)
+            if c >= 4:
+                steady.append((t0, t1))
+            if (li, c) in checks:
+                got = to64(out[rows])
+                vis = model.present_chunks()
+                kv = [chunk_qkv_device(sh, cfg, li, x)[1:] for x in vis]
+                kk = np.concatenate([to64(a) for a, _ in kv])
+                vv = np.concatenate([to64(b) for _, b in kv])
+                want = oatt.attention_rows(to64(q), kk, vv, scale, rows)
+                assert_close(got, want, ATOL_BF16, RELL2_BF16, f"layer {li} chunk {c}")
+    torch.cuda.synchronize()
+    for li, cache in enumerate(caches):
+        assert cache.chunk_of_region == [0, 319, 317, 318]  # slot (c - 1) mod 3
+        for x in (0, 317, 318, 319):
+            _, k, v = chunk_qkv_device(sh, cfg, li, x)
+            r = cache.chunk_of_region.index(x)
+            sl = slice(r * sh.chunk_tokens, (r + 1) * sh.chunk_tokens)
+            assert torch.equal(cache.k[sl], k) and torch.equal(cache.v[sl], v), (li, x)
+        assert cache.last_device_error() == swl.KVC_OK
+    ms = float(np.mean([a.elapsed_time(b) for a, b in steady]))
+    print(f"rolling stream: {ms:.4f} ms per layer-step, "
+          f"{sh.chunk_frames / ms * 1e3:.1f} latent frames/s per layer (steady state)")
 
 
 def test_state_machine_matches_oracle(swl):
