@@ -78,7 +78,9 @@ def _src_sha(name):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi every 10 ms with a timestamp; stop() keeps the samples that
+    fall inside the timed window (all samples if none does, flagged)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -90,12 +92,13 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.dev)],
+                 "-lms", "10", "-i", str(self.dev)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float | None = None, t1: float | None = None):
+        """t0, t1: the timed window in time.time() seconds."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -104,23 +107,24 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        from datetime import datetime
+        rows = []
         for line in out.splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower().startswith("active")}
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None, "reasons": sorted(reasons),
+                "samples": len(use), "in_timed_window": bool(inside)}
 
 
 # ---------------------------------------------------------------------------
@@ -362,27 +366,29 @@ def main():
     # FP4 append (amax, encode), FP4 attention; evict without scrub launches nothing
     launches_per_step = 3 + 1 + 1 + 2 + 1
 
-    for i in range(args.warmup):
-        step(layers[i % nlayers])
-    torch.cuda.synchronize()
-
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
           for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else local)
+    sampler.start()
+    time.sleep(0.3)  # the sampler's first readings, before the GPU work below
+    # warm-up right before the timed steps: no idle gap in between
+    for i in range(args.warmup):
+        step(layers[i % nlayers])
+    torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take a first reading
+    t_epoch0 = time.time()
     t_wall = time.perf_counter()
     for s in range(args.steps):
         step(layers[(args.warmup + s) % nlayers], ev[s])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    t_epoch1 = time.time()
     if dist:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_epoch0, t_epoch1)
 
     row_ms = {r: 0.0 for r in ROWS}
     total_ms = 0.0
