@@ -232,12 +232,6 @@ __device__ __forceinline__ void encode_block(const uint32_t (&w)[8], float g, co
 // ---------------------------------------------------------------------------
 // The encode pass re-reads the input the amax pass just streamed; a K/V chunk
 // (2 x 14.4 MB for the LongLive-1.3B layer shape) fits the 126 MB L2.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-// wait until the previous grid in the stream has completed and its memory is visible
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 __device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint4 v) {
   return bf16x2_max_abs(acc, bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w)));
 }

@@ -343,4 +343,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Programmatic dependent launch.  launch_dependents: the next grid in the
+// stream, if launched with the programmatic-serialisation attribute, may start
+// once every CTA of this grid has issued it (or exited).  wait: block until the
+// previous grid in the stream has completed and its memory is visible (returns
+// at once when this grid was launched without the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace kvc
