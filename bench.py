@@ -278,6 +278,24 @@ def hbm_kernels(swl, dev, layers, randn, per_graph: int = 8, replays: int = 6):
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank bookkeeping (replicas: every rank runs the same step on its GPU)
+# ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The job's time for a weak-scaled step: the slowest rank's."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return flop_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def main():
@@ -396,12 +414,9 @@ def main():
         total_ms += ev[s][0].elapsed_time(ev[s][-1])
         for i, r in enumerate(ROWS):
             row_ms[r] += ev[s][i].elapsed_time(ev[s][i + 1])
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = STEP_FLOP * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(STEP_FLOP, world, ms_per_step)
 
     # ---- end to end through the public API with host buffers.  Every step's
     # inputs come from pinned host memory and its two attention outputs go back
@@ -460,11 +475,8 @@ def main():
     e_end.record(comp)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end) / n_e2e
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = STEP_FLOP * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_tflops(STEP_FLOP, world, e2e_ms)
 
     hbm = hbm_kernels(swl, dev, layers, randn)
 
