@@ -540,6 +540,21 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     bool ok = true;
     int kv_region = -1;  // FP4: region whose tensor scales are held below
     float kv_kg = 0.0f, kv_vg = 0.0f;
+    // FP4: P is stored as f16 times the region's V tensor scale, and P itself
+    // reaches 2^8 under a held running max.  Every region's V scale is divided
+    // by one power of two G >= the largest visible one, so that product lies
+    // in [0, 2^8] whatever the magnitude of V (no f16 overflow for large V, no
+    // subnormal P for small V); G returns in the final normalisation (exact).
+    [[maybe_unused]] float v_shift = 1.0f, inv_v_shift = 1.0f;
+    if constexpr (kFp4) {
+      float gmax = 0.0f;
+      for (int s2 = 0; s2 < p.nseg; ++s2) gmax = fmaxf(gmax, __ldg(p.vg + p.seg_region[s2]));
+      if (gmax > 0.0f && gmax < 1.0e36f) {  // a tensor scale is at most 3.39e38 / 2688
+        const int e = max(-125, ((int)((__float_as_uint(gmax) >> 23) & 0xFFu)) - 126);  // gmax < 2^e
+        v_shift = __uint_as_float((uint32_t)(127 + e) << 23);
+        inv_v_shift = __uint_as_float((uint32_t)(127 - e) << 23);
+      }
+    }
     while (ok && sh.next(p, pc)) {
       const int h = pc.u / p.n_pairs;
       const int m0 = (pc.u % p.n_pairs) * (2 * BM);
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           if (region != kv_region) {  // consecutive tiles mostly share a region
             kv_region = region;
             kv_kg = __ldg(p.kg + region);
-            kv_vg = __ldg(p.vg + region);
+            kv_vg = __ldg(p.vg + region) * inv_v_shift;
           }
           const float cg = c * kv_kg;
           const float gv = kv_vg;
@@ -765,6 +780,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       } else if (head) {
         inv_l = 1.0f / l;
       }
+      if constexpr (kFp4) inv_l *= v_shift;
       float* wsw = nullptr;  // this piece handed to CTA g-1 (!head)
       if (!head) {
         wsw = p.ws_o + ((size_t)g * 2 * BM + prow) * D;

@@ -124,12 +124,12 @@ def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
 @pytest.mark.parametrize("where", ["every_tile", "late_tile"])
 def test_fp4_max_jump_within_tile(swl, where):
     """Keys 64..127 of a 128-key tile whose logits lie more than 2^8 (log2
-    units) above those of keys 0..63: the softmax moves its reference in the
-    middle of the tile and rescales the P it already wrote for the first half.
-    256-token chunks = two tiles each; queries 10u + noise, planted keys 10u
-    (u a unit vector).  every_tile: the jump comes on each piece's first tile;
-    late_tile: only the last tile of chunk 2 has it, after other tiles set the
-    reference."""
+    units) above those of keys 0..63 and of the tiles before: the softmax must
+    move its held reference maximum (and rescale O) before forming that tile's
+    P.  256-token chunks = two tiles each; queries 10u + noise, planted keys
+    10u (u a unit vector).  every_tile: the jump comes on each piece's first
+    tile; late_tile: only the last tile of chunk 2 has it, after other tiles
+    set the reference."""
     H, D, Tc, W = 2, 128, 256, 2
     rng = np.random.default_rng(31)
     u = rng.standard_normal(D)
@@ -155,6 +155,36 @@ def test_fp4_max_jump_within_tile(swl, where):
     torch.cuda.synchronize()
     want = oatt.sinkwin_attention(model, bf16_to_f64(qb), scale)
     assert_close(to64(out), want, ATOL_FP4, None, f"fp4 max jump ({where})", plus_output_rounding=True)
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+@pytest.mark.parametrize("vmag", [2.0 ** -14, 2.0 ** 26])
+def test_fp4_v_magnitude_extremes(swl, vmag):
+    """P is stored as f16 times the V tensor scale g_V (up to 2^8 under a held
+    running max).  V of magnitude 2^-14 (g_V ~ 1e-7: f16 subnormal products) or
+    2^26 (g_V ~ 1e5: beyond the f16 range) must give the oracle's output scaled
+    by the same factor; the three regions' V differ by 2^-3 per chunk, so the
+    regions' g_V differ too.  Compared after dividing by the magnitude (a power
+    of two, exact)."""
+    H, D, W = 2, 128, 2
+    rng = np.random.default_rng(41)
+    cache = swl.KVCache(H, D, 128, 1, W, dtype="fp4")
+    model = CacheModel(H, D, 128, W)
+    for c in range(1 + W):
+        k = rng.standard_normal((128, H, D))
+        v = rng.standard_normal((128, H, D)) * (vmag * 2.0 ** (-3 * c))
+        kb = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16)
+        vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+        cache.append(kb.cuda(), vb.cuda(), c)
+        model.append(c, ofp4.dequantize(*ofp4.quantize(_f32(kb))), ofp4.dequantize(*ofp4.quantize(_f32(vb))))
+    q = rng.standard_normal((200, H, D))
+    qb = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    out = cache.attn(qb.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(qb), scale)
+    assert_close(to64(out) / vmag, want / vmag, ATOL_FP4, None, f"fp4 |V| ~ {vmag:g}",
+                 plus_output_rounding=True)
     assert cache.last_device_error() == swl.KVC_OK
 
 
