@@ -131,9 +131,14 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
  * sink region plus every occupied window slot (no mask inside that set; keys are
  * read in physical order, which softmax does not see).  q, out: device bf16
  * [tq][H][D]; tq >= 0 (0 is a no-op); softmax_scale finite and >= 0 (else
- * KVC_EINVAL).  FP4 caches are dequantised inside the tile load.  Attention supports D in {64, 128} (else KVC_EUNSUPPORTED); the sink
- * must be present (else KVC_ESTATE).  A kernel wait that runs out leaves
- * KVC_ETIMEOUT for kvc_last_device_error. */
+ * KVC_EINVAL).  D in {64, 128} (else KVC_EUNSUPPORTED); the sink must be
+ * present (else KVC_ESTATE).  A kernel wait that runs out leaves KVC_ETIMEOUT
+ * for kvc_last_device_error.
+ * Arithmetic: bf16 operands, fp32 accumulation and softmax, bf16 output.  FP4
+ * caches are dequantised inside the tile load, exactly: K as e2m1 * s (bf16),
+ * V as e2m1 * s (f16); the regions' fp32 tensor scales enter the logit scale
+ * (K) and P (V, P stored as f16 after dividing every V scale by one power of
+ * two covering the largest, so any finite magnitude of V is representable). */
 int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
                      float softmax_scale, kvc_stream_t stream);
 
