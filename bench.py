@@ -52,8 +52,8 @@ WORKLOAD = ("LongLive-1.3B layer chunk step: 12 heads x 128, 4680 queries/chunk,
 TRAFFIC = {
     # ncu --set full on the LongLive-1.3B layer workload (one launch each);
     # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
-    "sinkwin_attn_kernel<128,false>": {"bytes": 308647680 + 26215680, "src_sha": "26fc0ad55d0a8ed3"},
-    "sinkwin_attn_kernel<128,true>": {"bytes": 48041472 + 4368128, "src_sha": "26fc0ad55d0a8ed3"},
+    "sinkwin_attn_kernel<128,false>": {"bytes": 309258240 + 26184960, "src_sha": "e2953c2cbf9151d6"},
+    "sinkwin_attn_kernel<128,true>": {"bytes": 48115200 + 4129024, "src_sha": "e2953c2cbf9151d6"},
 }
 
 
