@@ -3,6 +3,7 @@ CUDA path (through the C ABI) against the float64 oracle on the same inputs."""
 
 import math
 import random
+import time
 
 import numpy as np
 import pytest
@@ -212,6 +213,9 @@ def test_rolling_stream_30_layers_320_chunks(swl):
     slot_maps = [CacheModel(1, 1, 1, W) for _ in range(n_layers)]  # slot rule only
     z1 = np.zeros((1, 1, 1))
     steady = []
+    checked_s = 0.0  # host time spent on the sampled oracle checks (excluded from the wall time)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
     for c in range(n_chunks):
         for li in range(n_layers):
             q, k, v = chunk_qkv_device(sh, cfg, li, c)
@@ -230,6 +234,7 @@ def test_rolling_stream_30_layers_320_chunks(swl):
             if c >= 4:
                 steady.append((t0, t1))
             if (li, c) in checks:
+                t_chk = time.perf_counter()
                 got = to64(out[rows])
                 vis = model.present_chunks()
                 kv = [chunk_qkv_device(sh, cfg, li, x)[1:] for x in vis]
@@ -237,7 +242,9 @@ def test_rolling_stream_30_layers_320_chunks(swl):
                 vv = np.concatenate([to64(b) for _, b in kv])
                 want = oatt.attention_rows(to64(q), kk, vv, scale, rows)
                 assert_close(got, want, ATOL_BF16, RELL2_BF16, f"layer {li} chunk {c}")
+                checked_s += time.perf_counter() - t_chk
     torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall - checked_s
     for li, cache in enumerate(caches):
         assert cache.chunk_of_region == [0, 319, 317, 318]  # slot (c - 1) mod 3
         for x in (0, 317, 318, 319):
@@ -248,7 +255,9 @@ def test_rolling_stream_30_layers_320_chunks(swl):
         assert cache.last_device_error() == swl.KVC_OK
     ms = float(np.mean([a.elapsed_time(b) for a, b in steady]))
     print(f"rolling stream: {ms:.4f} ms per layer-step, "
-          f"{sh.chunk_frames / ms * 1e3:.1f} latent frames/s per layer (steady state)")
+          f"{sh.chunk_frames / ms * 1e3:.1f} latent frames/s per layer (steady state); "
+          f"whole stream {wall:.2f} s wall including input generation "
+          f"({n_chunks * sh.chunk_frames} latent frames x {n_layers} layers)")
 
 
 def test_state_machine_matches_oracle(swl):
