@@ -13,8 +13,18 @@ from . import _abi
 from ._abi import KVC_BF16, KVC_FP4, KvcCache, check, lib
 
 
-def _stream(stream=None) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
+def _cuda_device(device) -> torch.device:
+    d = torch.device(device)
+    if d.type != "cuda":
+        raise ValueError(f"expected a CUDA device, got {d}")
+    return torch.device("cuda", torch.cuda.current_device() if d.index is None else d.index)
+
+
+def _stream(device: torch.device, stream=None) -> ctypes.c_void_p:
+    """The given stream (which must belong to `device`), else `device`'s current one."""
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if s.device != device:
+        raise ValueError(f"stream on {s.device}, tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -22,9 +32,10 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
-def _require(t: torch.Tensor, dtype, shape, name: str):
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
-        raise ValueError(f"{name}: expected contiguous CUDA {dtype} {tuple(shape)}, "
+def _require(t: torch.Tensor, dtype, shape, name: str, device: torch.device):
+    if (t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous()
+            or t.device != device):
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)} on {device}, "
                          f"got {t.dtype} {tuple(t.shape)} on {t.device}")
 
 
@@ -45,7 +56,7 @@ class KVCache:
         c.dtype = {"bf16": KVC_BF16, "fp4": KVC_FP4}[dtype]
         c.scrub_on_evict = 1 if scrub_on_evict else 0
         self.dtype = dtype
-        self.device = torch.device(device)
+        self.device = _cuda_device(device)
         self.H, self.D = heads, head_dim
         self.Tc = tokens_per_frame * chunk_frames
         self.W = window_chunks
@@ -88,25 +99,31 @@ class KVCache:
         return [int(self.c.chunk_of_region[i]) for i in range(1 + self.W)]
 
     # -- calls ---------------------------------------------------------------
+    # Every call runs with the cache's device current and on that device's stream:
+    # the library launches on the current device, with the pointers it is given.
     def append(self, k: torch.Tensor, v: torch.Tensor, chunk_idx: int, stream=None) -> None:
         shp = (self.Tc, self.H, self.D)
-        _require(k, torch.bfloat16, shp, "k")
-        _require(v, torch.bfloat16, shp, "v")
-        check(lib().kvc_append(ctypes.byref(self.c), _ptr(k), _ptr(v), int(chunk_idx), _stream(stream)),
-              "kvc_append")
+        _require(k, torch.bfloat16, shp, "k", self.device)
+        _require(v, torch.bfloat16, shp, "v", self.device)
+        with torch.cuda.device(self.device):
+            check(lib().kvc_append(ctypes.byref(self.c), _ptr(k), _ptr(v), int(chunk_idx),
+                                   _stream(self.device, stream)), "kvc_append")
 
     def evict(self, chunk_idx: int, stream=None) -> None:
-        check(lib().kvc_evict(ctypes.byref(self.c), int(chunk_idx), _stream(stream)), "kvc_evict")
+        with torch.cuda.device(self.device):
+            check(lib().kvc_evict(ctypes.byref(self.c), int(chunk_idx), _stream(self.device, stream)),
+                  "kvc_evict")
 
     def attn(self, q: torch.Tensor, softmax_scale: float, out: torch.Tensor | None = None,
              stream=None) -> torch.Tensor:
         tq = q.shape[0]
-        _require(q, torch.bfloat16, (tq, self.H, self.D), "q")
+        _require(q, torch.bfloat16, (tq, self.H, self.D), "q", self.device)
         if out is None:
             out = torch.empty_like(q)
-        _require(out, torch.bfloat16, (tq, self.H, self.D), "out")
-        check(lib().sinkwin_attn(ctypes.byref(self.c), _ptr(q), _ptr(out), int(tq),
-                                 float(softmax_scale), _stream(stream)), "sinkwin_attn")
+        _require(out, torch.bfloat16, (tq, self.H, self.D), "out", self.device)
+        with torch.cuda.device(self.device):
+            check(lib().sinkwin_attn(ctypes.byref(self.c), _ptr(q), _ptr(out), int(tq),
+                                     float(softmax_scale), _stream(self.device, stream)), "sinkwin_attn")
         return out
 
     def recache(self, hidden: torch.Tensor, w_kv: torch.Tensor, gamma: torch.Tensor | None,
@@ -114,17 +131,19 @@ class KVCache:
                 stream=None) -> None:
         n = len(chunk_ids)
         HD = self.H * self.D
-        _require(hidden, torch.bfloat16, (n * self.Tc, HD), "hidden")
-        _require(w_kv, torch.bfloat16, (HD, 2 * HD), "w_kv")
+        _require(hidden, torch.bfloat16, (n * self.Tc, HD), "hidden", self.device)
+        _require(w_kv, torch.bfloat16, (HD, 2 * HD), "w_kv", self.device)
         if gamma is not None:
-            _require(gamma, torch.float32, (HD,), "gamma")
+            _require(gamma, torch.float32, (HD,), "gamma", self.device)
         ids = (ctypes.c_int64 * n)(*[int(x) for x in chunk_ids])
-        check(lib().kvc_recache(ctypes.byref(self.c), _ptr(hidden), _ptr(w_kv), _ptr(gamma),
-                                float(eps), ids, n, int(grid_h), int(grid_w), float(theta),
-                                _stream(stream)), "kvc_recache")
+        with torch.cuda.device(self.device):
+            check(lib().kvc_recache(ctypes.byref(self.c), _ptr(hidden), _ptr(w_kv), _ptr(gamma),
+                                    float(eps), ids, n, int(grid_h), int(grid_w), float(theta),
+                                    _stream(self.device, stream)), "kvc_recache")
 
     def last_device_error(self, stream=None) -> int:
-        return int(lib().kvc_last_device_error(ctypes.byref(self.c), _stream(stream)))
+        with torch.cuda.device(self.device):
+            return int(lib().kvc_last_device_error(ctypes.byref(self.c), _stream(self.device, stream)))
 
 
 def quant_fp4(x: torch.Tensor, stream=None):
@@ -132,11 +151,13 @@ def quant_fp4(x: torch.Tensor, stream=None):
     scales u8 [n/16], gscale f32 [1])."""
     if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA bf16 tensor")
+    dev = _cuda_device(x.device)
     n = x.numel()
     codes = torch.empty(n // 2, dtype=torch.uint8, device=x.device)
     scales = torch.empty(n // 16, dtype=torch.uint8, device=x.device)
     g = torch.empty(1, dtype=torch.float32, device=x.device)
     ws = torch.empty(_abi.KVC_QUANT_WS_WORDS, dtype=torch.int32, device=x.device)
-    check(lib().kvc_quant_fp4(_ptr(x), int(n), _ptr(codes), _ptr(scales), _ptr(g), _ptr(ws),
-                              _stream(stream)), "kvc_quant_fp4")
+    with torch.cuda.device(dev):
+        check(lib().kvc_quant_fp4(_ptr(x), int(n), _ptr(codes), _ptr(scales), _ptr(g), _ptr(ws),
+                                  _stream(dev, stream)), "kvc_quant_fp4")
     return codes, scales, g

@@ -122,3 +122,22 @@ def test_quant_and_watchdog_validation(lib):
     assert lib.kvc_watchdog_selftest(None, 10, None) == _abi.KVC_EINVAL
     assert lib.kvc_watchdog_selftest(x, 0, None) == _abi.KVC_EINVAL
     assert lib.kvc_status_string(_abi.KVC_ESTATE).decode().startswith("invalid in")
+
+
+def test_binding_rejects_tensors_off_the_cache_device():
+    """The binding checks dtype, shape, contiguity and device before any call:
+    a host tensor, a tensor on another GPU or a strided view never reaches the
+    library (its kernels would be handed a foreign pointer)."""
+    import torch
+    from sink_short_window_sinkwin_b300 import cache as cb
+    dev = torch.device("cuda", 0)
+    good = torch.empty(2, 3, dtype=torch.bfloat16, device="meta")
+    with pytest.raises(ValueError, match="on cuda:0"):
+        cb._require(torch.zeros(2, 3, dtype=torch.bfloat16), torch.bfloat16, (2, 3), "x", dev)
+    with pytest.raises(ValueError):
+        cb._require(good, torch.float32, (2, 3), "x", dev)
+    with pytest.raises(ValueError):
+        cb._require(torch.zeros(3, 2, dtype=torch.bfloat16).t(), torch.bfloat16, (2, 3), "x", dev)
+    with pytest.raises(ValueError, match="CUDA device"):
+        cb._cuda_device("cpu")
+    assert cb._cuda_device("cuda:1") == torch.device("cuda", 1)
