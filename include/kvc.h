@@ -68,10 +68,12 @@ typedef enum { KVC_BF16 = 0, KVC_FP4 = 1 } kvc_dtype;
 
 typedef struct kvc_cache {
   /* ---- geometry: set by the caller before kvc_init ---- */
-  int32_t heads;            /* H >= 1 */
-  int32_t head_dim;         /* D, a multiple of 16; attention supports 64 and 128 */
+  int32_t heads;            /* H, 1..65536 */
+  int32_t head_dim;         /* D, a multiple of 16 up to 256; attention supports 64 and 128 */
   int32_t tokens_per_frame; /* latent tokens of one frame (1560 = 30 x 52 for LongLive-1.3B) */
-  int32_t chunk_frames;     /* frames per chunk; the sink is exactly one chunk */
+  int32_t chunk_frames;     /* frames per chunk; the sink is exactly one chunk.  The cache's
+                               rows (1 + W) * tokens_per_frame * chunk_frames are at most
+                               2^30, and rows * H * D at most 2^40 (else KVC_EINVAL) */
   int32_t window_chunks;    /* W, 1..KVC_MAX_WINDOW ring slots, the current chunk included */
   int32_t dtype;            /* kvc_dtype */
   /* ---- device buffers: caller-allocated, sizes from kvc_cache_bytes ---- */

@@ -93,6 +93,7 @@ using namespace kvc;
 namespace {
 
 constexpr int32_t kMaxRows = 1 << 30;
+constexpr int32_t kMaxHeads = 1 << 16;
 
 int64_t chunk_tokens(const kvc_cache* c) { return (int64_t)c->tokens_per_frame * c->chunk_frames; }
 int64_t cache_rows(const kvc_cache* c) { return (1 + (int64_t)c->window_chunks) * chunk_tokens(c); }
@@ -103,8 +104,10 @@ bool geometry_ok(const kvc_cache* c) {
   if (c->tokens_per_frame < 1 || c->chunk_frames < 1) return false;
   if (c->window_chunks < 1 || c->window_chunks > KVC_MAX_WINDOW) return false;
   if (c->dtype != KVC_BF16 && c->dtype != KVC_FP4) return false;
+  // bound each factor before the products below, so none of them can overflow
+  if (c->heads > kMaxHeads || chunk_tokens(c) > kMaxRows) return false;
   const int64_t S = cache_rows(c);
-  if (S <= 0 || S > kMaxRows) return false;
+  if (S > kMaxRows) return false;
   if (S * c->heads * (int64_t)c->head_dim > (int64_t(1) << 40)) return false;
   return true;
 }

@@ -80,6 +80,16 @@ def test_init_validation(lib):
     assert lib.kvc_init(ctypes.byref(f)) == _abi.KVC_EINVAL
 
 
+def test_geometry_products_cannot_overflow(lib):
+    """Geometries whose row count or element count would overflow 64-bit
+    arithmetic (int32 fields near 2^31) are rejected, not wrapped."""
+    big = 2 ** 31 - 1
+    for kw in (dict(tpf=big, cf=big), dict(tpf=big, cf=2), dict(H=big), dict(H=big, tpf=big, cf=big)):
+        b = _cache(**kw)
+        assert lib.kvc_cache_bytes(ctypes.byref(b), 0) == 0, kw
+        assert lib.kvc_init(ctypes.byref(b)) == _abi.KVC_EINVAL, kw
+
+
 def test_rejections_change_nothing(lib):
     c = _cache(H=1, D=64, tpf=16, cf=2, W=2)
     assert lib.kvc_init(ctypes.byref(c)) == _abi.KVC_OK
