@@ -40,3 +40,11 @@ def test_oracle_does_not_use_the_library():
     pat = re.compile(r"sink_short_window_sinkwin_b300|libsinkwin|ctypes")
     for path in _sources(os.path.join(ROOT, "oracle"), (".py",)):
         assert not pat.search(open(path, encoding="utf-8").read()), f"{path} touches the library"
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libsinkwin.so the binding refuses to load: there is no fallback."""
+    import pytest
+    from sink_short_window_sinkwin_b300 import _abi
+    with pytest.raises(ImportError, match="missing"):
+        _abi.load(str(tmp_path / "libsinkwin.so"))
