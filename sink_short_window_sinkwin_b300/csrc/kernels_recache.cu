@@ -39,7 +39,7 @@ struct GemmParams {
   int32_t rows, HD, Tc;
   int32_t col0;    // first output column of this launch in [K | V]: 0 (K) or HD (V)
   int32_t ncol;    // column tiles (HD / BN)
-  int32_t ntiles;  // tile groups: ceil(row tiles / cluster size) x column tiles
+  int32_t ntiles;  // row tiles x column tiles
   int32_t region[kMaxSeg];
   __nv_bfloat16* k;
   __nv_bfloat16* v;
@@ -68,42 +68,32 @@ struct __align__(1024) GemmSmem {
   uint32_t stage[4][32][32];
 };
 
-// Persistent, in clusters of kC CTAs.  A tile group is kC consecutive row tiles
-// x one column tile; cluster c takes groups c, c + NC, ... (row-major over
-// [row group][column tile], so consecutive groups share hidden rows through
-// L2) and its CTA of rank r computes row tile (group row) * kC + r.  The kC
-// CTAs of a group need the same B tile: each loads its own A tile and a 1/kC
-// share of B, multicast into every CTA of the cluster, which cuts the L2 -> SM
-// operand traffic per tile by a third (kC = 2).  A ring
-// stage is refilled only once the MMAs of all kC CTAs have consumed it, so its
-// empty barrier counts kC commits (each CTA commits to all of them).  Row tiles
-// past the last row load as TMA zero fill and store nothing.  The accumulator
-// alternates between two TMEM buffers, so the epilogue of one tile overlaps the
-// MMAs of the next.
+// Persistent: one CTA per SM.  Tiles are row-major over [row tile][column
+// tile], CTA c takes tiles c, c + G, ... (so concurrent CTAs share hidden rows
+// and weight columns through L2).  Every CTA loads its own A and B tiles into
+// its own shared memory.  Row tiles past the last row load as TMA zero fill and
+// store nothing.  The accumulator alternates between two TMEM buffers, so the
+// epilogue of one tile overlaps the MMAs of the next.
 // kKf32: K launch (fp32 rows parked in the K|V rows); else the V launch (bf16).
-template <int BN, bool kKf32, int kC>
+template <int BN, bool kKf32>
 __global__ void __launch_bounds__(kRThreads, 1)
     recache_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
-  static_assert(kC == 1 || kC == 2, "cluster size");
-  static_assert((BN / 64) % kC == 0, "each CTA loads whole 64-column boxes of B");
   using Smem = GemmSmem<BN>;
   constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
-  constexpr uint16_t kMask = (uint16_t)((1u << kC) - 1u);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.HD / RK;
-  const int rank = kC > 1 ? (int)cluster_ctarank() : 0;
-  const int cid = blockIdx.x / kC, ncl = gridDim.x / kC;  // cluster index, clusters
-  // row tile and first column of tile group t for this CTA
-  auto tile_m0 = [&](int t) { return ((t / p.ncol) * kC + rank) * RM; };
+  const int cid = blockIdx.x, ncl = gridDim.x;
+  // row tile and first column of tile t
+  auto tile_m0 = [&](int t) { return (t / p.ncol) * RM; };
   auto tile_n0 = [&](int t) { return (t % p.ncol) * BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.bar_full[s], 1);
-      mbar_init(&sm.bar_empty[s], kC);
+      mbar_init(&sm.bar_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.bar_acc_full[b], 1);
@@ -119,9 +109,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // the other CTAs' multicast copies and commits target this CTA's barriers:
-  // every CTA of the cluster initialises its barriers before any is used
-  if constexpr (kC > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const Watchdog wd{&sm.abort_flag, p.dev_err};
@@ -140,33 +127,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
             ok = false;
             break;
           }
-          // this CTA's A tile plus the whole B tile (its own share and the
-          // shares the other CTAs of the cluster multicast here)
           mbar_expect_tx(&sm.bar_full[s], RM * RK * 2 + RK * BN * 2);
           tma_load_2d(&sm.a[s][0], &tmA, &sm.bar_full[s], kb * RK, m0);
-          constexpr int kBoxes = BN / 64 / kC;  // B boxes this CTA loads
 #pragma unroll
-          for (int q = 0; q < kBoxes; ++q) {
-            const int nb = rank * kBoxes + q;
-            if constexpr (kC > 1)
-              tma_load_2d_mc(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK, kMask);
-            else
-              tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
-          }
+          for (int nb = 0; nb < BN / 64; ++nb)
+            tma_load_2d(&sm.b[s][nb][0], &tmB, &sm.bar_full[s], p.col0 + nloc + nb * 64, kb * RK);
         }
       }
       if (sm.abort_flag) {  // every copy this thread started lands before the CTA exits
         for (int s = 0; s < kStages; ++s) {
           const int cnt = issued > s ? (issued - s + kStages - 1) / kStages : 0;
           if (cnt) mbar_drain(&sm.bar_full[s], (cnt - 1) & 1);
-        }
-      }
-      if constexpr (kC > 1) {
-        // the last commits of every stage (from all kC CTAs, some remote) have
-        // arrived before this CTA's shared memory goes away
-        for (int s = 0; s < kStages; ++s) {
-          const int cnt = issued > s ? (issued - s + kStages - 1) / kStages : 0;
-          if (cnt) mbar_drain(&sm.bar_empty[s], (cnt - 1) & 1);
         }
       }
     }
@@ -194,10 +165,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             const uint64_t bd = sdesc_sw128(smem_u32(&sm.b[s][0][0]) + kk * 2048, RK * 128, 1024);
             mma_bf16_ss(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (kC > 1)
-            mma_commit_mc(&sm.bar_empty[s], kMask);  // frees the stage in every CTA of the cluster
-          else
-            mma_commit(&sm.bar_empty[s]);
+          mma_commit(&sm.bar_empty[s]);  // frees the stage for the producer
         }
         if (ok) mma_commit(&sm.bar_acc_full[buf]);
       }
@@ -376,88 +344,23 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
   }
 }
 
-// Whole clusters that can be resident at once for a kC-CTA cluster launch of
-// this kernel (0 if none).
-template <int BN, bool kKf32, int kC>
-int clusters_that_fit() {
-  static int cache[64] = {};  // per device; -1: queried, none fit
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev]) return cache[dev] > 0 ? cache[dev] : 0;
-  auto kern = recache_gemm_kernel<BN, kKf32, kC>;
+// One CTA per SM (persistent), never more CTAs than tiles.
+template <int BN, bool kKf32>
+cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
+                        cudaStream_t st) {
   const size_t smem = sizeof(GemmSmem<BN>) + 1024;
-  static bool smem_set[64] = {};
-  int fit = 0;
-  if (set_smem_once(kern, smem, smem_set) == cudaSuccess) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(attn_sm_count() / kC * kC), 1, 1);
-    cfg.blockDim = dim3(kRThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kC;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) fit = 0;
-  }
-  (void)cudaGetLastError();
-  cache[dev] = fit > 0 ? fit : -1;
-  return fit;
-}
-
-template <int BN, bool kKf32, int kC>
-cudaError_t launch_gemm_c(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
-                          cudaStream_t st) {
-  const size_t smem = sizeof(GemmSmem<BN>) + 1024;
-  auto kern = recache_gemm_kernel<BN, kKf32, kC>;
+  auto kern = recache_gemm_kernel<BN, kKf32>;
   static bool smem_set[64] = {};  // one per instantiation of this launcher
   cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
   const int nsm = attn_sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   p.ncol = p.HD / BN;
-  const int row_tiles = (rows + RM - 1) / RM;
-  p.ntiles = ((row_tiles + kC - 1) / kC) * p.ncol;
-  cudaLaunchConfig_t cfg{};
-  cfg.blockDim = dim3(kRThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // one CTA per SM, as many whole clusters as fit at once (persistent)
-  int clusters = nsm / kC;
-  if constexpr (kC > 1) {
-    const int fit = clusters_that_fit<BN, kKf32, kC>();
-    if (fit < 1) return cudaErrorNotSupported;
-    clusters = fit < clusters ? fit : clusters;
-  }
-  if (clusters > p.ntiles) clusters = p.ntiles;
-  if (clusters < 1) clusters = 1;
-  cfg.gridDim = dim3(clusters * kC, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
-}
-
-// B is shared by clusters of 2 CTAs (whole 64-column boxes each) when such
-// clusters still cover (nearly) every SM; otherwise the plain kernel.  Clusters
-// of 4 would halve the B traffic rather than cut it by a third, but on a B300
-// only 33 of them (132 SMs) can be resident at once, which costs more than the
-// shared B saves.
-template <int BN, bool kKf32>
-cudaError_t launch_gemm(int rows, const CUtensorMap& ta, const CUtensorMap& tb, GemmParams p,
-                        cudaStream_t st) {
-  const int nsm = attn_sm_count();
-  if constexpr (BN / 64 >= 2) {
-    if (clusters_that_fit<BN, kKf32, 2>() * 2 >= nsm - 2)
-      return launch_gemm_c<BN, kKf32, 2>(rows, ta, tb, p, st);
-  }
-  return launch_gemm_c<BN, kKf32, 1>(rows, ta, tb, p, st);
+  p.ntiles = ((rows + RM - 1) / RM) * p.ncol;
+  int grid = nsm < p.ntiles ? nsm : p.ntiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, kRThreads, smem, st>>>(ta, tb, p);
+  return cudaGetLastError();
 }
 
 template <int BN, int HD>

@@ -92,11 +92,11 @@ def test_recache_two_column_tiles_noncontiguous_positions(swl):
 
 
 @pytest.mark.parametrize("heads,head_dim", [(1, 128), (2, 128), (6, 128)])
-def test_recache_cluster_tile_widths(swl, heads, head_dim):
+def test_recache_tile_widths(swl, heads, head_dim):
     """H*D = 128, 256, 768: GEMM column tiles 128 or 256 wide (one, one and three
-    of them), the B tile shared by a 2-CTA cluster.  Three 120-token chunks are
-    three row tiles, so one CTA of the second cluster computes a row tile past
-    the last row (loaded as zeros, nothing stored)."""
+    of them).  Three 120-token chunks are 360 rows, so the last of the three
+    row tiles ends inside the tile (rows past the end load as zeros and store
+    nothing)."""
     sh = Shapes(heads, head_dim, 40, 3, 2, 4, 10)
     cache, model = _fill(swl, sh, 2)
     assert model.present_chunks() == [0, 1, 2]
