@@ -105,3 +105,28 @@ def recache(hidden, w_kv, gamma, chunk_ids, heads: int, head_dim: int,
         pf.append(f), ph.append(h), pw.append(w)
     k = rope3d(k, np.concatenate(pf), np.concatenate(ph), np.concatenate(pw), theta)
     return k, v
+
+
+def project_chunk(hidden, w_qkv, gamma_q, gamma_k, chunk_id: int, heads: int, head_dim: int,
+                  tokens_per_frame: int, chunk_frames: int, grid_w: int,
+                  eps: float = 1e-6, theta: float = 10000.0):
+    """Q, K, V [Tc][H][D] float64 of ONE new chunk, as the layer produces them
+    before they are attended to and appended.
+
+    LongLive summary page, 方法 (causal frame-level autoregression): each new
+    chunk's tokens are projected to queries, keys and values; the keys and
+    values join the cache every later chunk reads (§3 高效长推理, 帧汇聚点).
+    The same readings as ``recache`` hold (norm over the whole H*D row, then
+    3D RoPE at the chunk's absolute positions), applied to Q with its own gain:
+
+        [Q | K | V] = hidden @ w_qkv          (w_qkv [H*D][3*H*D], Q columns first)
+        Q = RoPE3D(RMSNorm(Q) * gamma_q),  K = RoPE3D(RMSNorm(K) * gamma_k)
+    """
+    x = np.asarray(hidden, dtype=np.float64) @ np.asarray(w_qkv, dtype=np.float64)
+    hd = heads * head_dim
+    Tc = x.shape[0]
+    f, h, w = token_positions(chunk_id, Tc, tokens_per_frame, chunk_frames, grid_w)
+    q = rope3d(rmsnorm(x[:, :hd], gamma_q, eps).reshape(Tc, heads, head_dim), f, h, w, theta)
+    k = rope3d(rmsnorm(x[:, hd:2 * hd], gamma_k, eps).reshape(Tc, heads, head_dim), f, h, w, theta)
+    v = x[:, 2 * hd:].reshape(Tc, heads, head_dim)
+    return q, k, v

@@ -237,3 +237,27 @@ def test_window_of_one_chunk_streams():
         m.append(c, z, z)  # overwrite while cached
         assert m.chunk_of_region == [0, c]
         assert m.present_chunks() == visible_chunks_of_step(c, 1)
+
+
+def test_attention_rows_against_brute_force_and_full_attention():
+    """attention_rows (the expected value of every sampled full-size parity
+    test) against pure-Python loops on a small case, and against the full
+    attention() for random row and head subsets, including heads=None."""
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((9, 3, 8))
+    k = rng.standard_normal((13, 3, 8))
+    v = rng.standard_normal((13, 3, 8))
+    rows, heads = [8, 0, 5], [2, 0]
+    got = oatt.attention_rows(q, k, v, 0.4, rows, heads)
+    brute = _brute_attention(q, k, v, 0.4)
+    assert got.shape == (3, 2, 8)
+    assert np.allclose(got, brute[rows][:, heads], rtol=0, atol=1e-13)
+    sh = LAYER_1P3B
+    q, k, v = (bf16_to_f64(t) for t in chunk_qkv(sh, 1, 0, 0, "rms1", q_rows=300))
+    full = oatt.attention(q, k, v, 1.0 / math.sqrt(sh.head_dim))
+    for trial in range(3):
+        rows = rng.choice(300, size=17, replace=False)
+        heads = None if trial == 0 else list(rng.choice(sh.heads, size=5, replace=False))
+        got = oatt.attention_rows(q, k, v, 1.0 / math.sqrt(sh.head_dim), rows, heads)
+        want = full[rows] if heads is None else full[rows][:, heads]
+        assert np.allclose(got, want, rtol=0, atol=1e-13)

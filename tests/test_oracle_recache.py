@@ -95,3 +95,40 @@ def test_recache_composition():
     # the norm is taken before the rotation: rotation keeps the row RMS
     assert np.allclose(np.sqrt(np.mean(k.reshape(-1, H * D) ** 2, axis=1)),
                        np.sqrt(np.mean(kn ** 2, axis=1)), atol=1e-12)
+
+
+def test_recache_equals_appended_chunk_projections():
+    """Recache => append consistency: project each chunk's hidden states as it
+    arrives (project_chunk, K and V appended to the cache model), stream past
+    evictions, then recache the present chunks from the same hidden states:
+    every cached row comes out the same.  The present chunks {0, 5, 6} sit at
+    non-adjacent frame positions, so a wrong position offset or chunk order in
+    either path shows."""
+    from oracle.cache_model import CacheModel
+    rng = np.random.default_rng(5)
+    H, D, tpf, cf, gw, W = 2, 64, 16, 2, 4, 2
+    Tc, HD = tpf * cf, H * D
+    w_qkv = rng.standard_normal((HD, 3 * HD)) * 0.05
+    gq, gk = rng.uniform(0.5, 1.5, HD), rng.uniform(0.5, 1.5, HD)
+    m = CacheModel(H, D, Tc, W)
+    hid = {}
+    for c in range(7):
+        hid[c] = rng.standard_normal((Tc, HD))
+        if c > W:
+            m.evict(c - W)
+        q, k, v = orc.project_chunk(hid[c], w_qkv, gq, gk, c, H, D, tpf, cf, gw)
+        assert q.shape == k.shape == v.shape == (Tc, H, D)
+        m.append(c, k, v)
+    ids = m.present_chunks()
+    assert ids == [0, 5, 6]
+    K0, V0 = m.physical()
+    k, v = orc.recache(np.concatenate([hid[c] for c in ids]), w_qkv[:, HD:], gk, ids, H, D, tpf,
+                       cf, gw)
+    m.recache(ids, k, v)
+    K1, V1 = m.physical()
+    assert np.allclose(K1, K0, rtol=0, atol=1e-12) and np.allclose(V1, V0, rtol=0, atol=1e-12)
+    # and Q is the K rule applied to the Q columns with Q's gain
+    q, _, _ = orc.project_chunk(hid[6], w_qkv, gq, gk, 6, H, D, tpf, cf, gw)
+    qq, _ = orc.recache(hid[6], np.concatenate([w_qkv[:, :HD], w_qkv[:, :HD]], axis=1), gq, [6],
+                        H, D, tpf, cf, gw)
+    assert np.allclose(q, qq, rtol=0, atol=1e-12)
