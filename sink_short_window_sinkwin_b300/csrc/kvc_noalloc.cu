@@ -10,11 +10,13 @@
 // the process exits, and allocates nothing.
 //
 // The array is a host-side stand-in in host code, not a device address: its
-// device address is looked up once per device with cudaGetSymbolAddress (with
-// that device current) and then passed to the kernels.
+// device address is looked up with cudaGetSymbolAddress, with the caller's
+// device current, on every call (a host-side lookup; the first one on a device
+// may load the library's device code there, so make the first call before any
+// stream capture) and then passed to the kernels.  Looking it up each time
+// keeps the address right after a cudaDeviceReset re-creates the device's
+// context and reloads the module.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "internal.h"
 #include "kvc.h"
@@ -27,23 +29,15 @@ static_assert(kQuantPartials <= KVC_NOALLOC_SCRATCH_WORDS, "scratch too small fo
 // one magnitude maximum per CTA of the encoder's first pass
 __device__ __align__(256) int32_t g_quant_scratch[KVC_NOALLOC_SCRATCH_WORDS];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_quant_scratch on the current device (looked up once).
-int32_t scratch_on_current_device(int32_t* status) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return *status = KVC_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return *status = KVC_EUNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_quant_scratch) != cudaSuccess || !p) return *status = KVC_ECUDA;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+// Device address of g_quant_scratch on the current device.
+int32_t* scratch_on_current_device(int32_t* status) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_quant_scratch) != cudaSuccess || !p) {
+    *status = KVC_ECUDA;
+    return nullptr;
   }
   *status = KVC_OK;
-  return dev;
+  return static_cast<int32_t*>(p);
 }
 
 }  // namespace
@@ -59,12 +53,12 @@ extern "C" int32_t kvc_quant_fp4_noalloc(const void* x, int64_t n, uint8_t* code
       (reinterpret_cast<uintptr_t>(gscale) & 3u))
     return KVC_EINVAL;
   int32_t st = KVC_OK;
-  const int dev = scratch_on_current_device(&st);
+  int32_t* scratch = scratch_on_current_device(&st);
   if (st != KVC_OK) return st;
   // The first pass writes every one of its kQuantPartials words before the
   // second pass reads them, so nothing has to be cleared between calls.
   QuantJob job{x, codes, scales, gscale};
-  return launch_quant_fp4(&job, 1, n, g_scratch_ptr[dev], reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_quant_fp4(&job, 1, n, scratch, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? KVC_OK
              : KVC_ECUDA;

@@ -29,10 +29,11 @@ def assert_close(got: np.ndarray, want: np.ndarray, atol: float, rel_l2: float |
     plus_output_rounding) and, if given, ||got - want|| / ||want|| <= rel_l2."""
     assert got.shape == want.shape, (what, got.shape, want.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    raw = float(np.abs(got - want).max()) if got.size else 0.0
     if plus_output_rounding:
         # subtract the output format's own rounding before the max-abs test
         err = np.maximum(np.abs(got - want) - bf16_half_ulp(want), 0.0)
-        what = what + " (beyond bf16 output rounding)"
+        what = what + f" (raw max-abs {raw:.3e}; beyond bf16 output rounding)"
     else:
         err = np.abs(got - want)
     mx = float(err.max()) if err.size else 0.0

@@ -2,6 +2,7 @@
 CUDA path (through the C ABI) against the float64 oracle on the same inputs."""
 
 import math
+import os
 import random
 import time
 
@@ -135,6 +136,90 @@ def test_many_items_full_compare(swl, workspace):
             torch.cuda.synchronize()
             want = oatt.sinkwin_attention(model, bf16_to_f64(qq), scale)
             assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"228 items, step {c}")
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def _planted_stream(swl, H, D, tpf, cf, W, where, seed, workspace=True):
+    """bf16 cache of 1 + W chunks whose keys are 0.3 N(0,1) except planted
+    rows 10u (u a unit vector); queries are 10u + 0.3 N(0,1).  A planted key's
+    logit lies about 12.7 (log2 units) above the others', beyond the 2^8 by
+    which the kernel lets its held row maximum go stale, so a tile that brings
+    the first planted keys of a piece forces the O rescale in TMEM.
+    where: "late_tile" plants keys only in the last tile of the newest chunk
+    (every earlier tile has set the held maximum low); "mid_chunk" plants them
+    in the second half of chunk 1 only."""
+    Tc = tpf * cf
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal(D)
+    u /= np.linalg.norm(u)
+    cache = swl.KVCache(H, D, tpf, cf, W, attn_workspace=workspace)
+    model = CacheModel(H, D, Tc, W)
+    for c in range(1 + W):
+        k = rng.standard_normal((Tc, H, D)) * 0.3
+        v = rng.standard_normal((Tc, H, D))
+        if where == "late_tile" and c == W:
+            k[Tc - 64:] = 10 * u
+        elif where == "mid_chunk" and c == 1:
+            k[Tc // 2:] = 10 * u
+        kb = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16)
+        vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+        cache.append(kb.cuda(), vb.cuda(), c)
+        model.append(c, bf16_to_f64(kb), bf16_to_f64(vb))
+    return cache, model, u, rng
+
+
+@pytest.mark.parametrize("where", ["late_tile", "mid_chunk"])
+def test_bf16_max_jump_rescales_o(swl, where):
+    """bf16 twin of the FP4 max-jump test: two heads, 256-token chunks (two
+    key tiles each), 130 queries, whole items visited from their first tile,
+    so the planted tile comes after tiles that set a low held maximum and the
+    kernel must rescale O (alpha = 2^-12 or so) before adding that tile."""
+    H, D = 2, 128
+    cache, model, u, rng = _planted_stream(swl, H, D, 128, 2, 2, where, 51)
+    q = 10 * u + 0.3 * rng.standard_normal((130, H, D))
+    qb = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    out = cache.attn(qb.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(qb), scale)
+    print(assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"bf16 max jump ({where})"))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_bf16_max_jump_split_items(swl):
+    """12 heads x 4680 queries = 228 items on 148 CTAs (step-balanced shares):
+    pieces with and without the planted keys hold maxima about 12 (log2 units)
+    apart, so both the in-TMEM rescale and the merge of two pieces with very
+    different maxima run."""
+    H, D = 12, 128
+    cache, model, u, rng = _planted_stream(swl, H, D, 100, 1, 2, "mid_chunk", 52)
+    q = 10 * u + 0.3 * rng.standard_normal((4680, H, D))
+    qb = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    out = cache.attn(qb.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, bf16_to_f64(qb), scale)
+    print(assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, "bf16 max jump, split items"))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_layer_attention_full_size_full_compare(swl):
+    """LongLive-1.3B layer at full size (4680 queries x 18720 keys x 12 heads,
+    RMS-1 rows so the softmax is far from uniform): every one of the
+    4680 x 12 x 128 outputs against the float64 oracle, which runs on all host
+    cores (oracle.pool)."""
+    from oracle.pool import attention_rows_parallel
+    sh = LAYER_1P3B
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    *_, (c, q, cache, model) = list(_stream(swl, sh, 1, 4, "rms1"))
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    got = to64(out)
+    kk, vv = model.visible_kv()
+    t0 = time.perf_counter()
+    want = attention_rows_parallel(bf16_to_f64(q), kk, vv, scale)
+    print(f"oracle: {time.perf_counter() - t0:.1f} s on {os.cpu_count()} CPUs")
+    print(assert_close(got, want, ATOL_BF16, RELL2_BF16, "layer full compare"))
     assert cache.last_device_error() == swl.KVC_OK
 
 

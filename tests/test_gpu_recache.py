@@ -123,6 +123,45 @@ def test_recache_layer_full_size_then_attention(swl):
     assert cache.last_device_error() == swl.KVC_OK
 
 
+def test_recache_equals_appended_projections(swl):
+    """Recache => append consistency on the GPU: stream chunks 0..6 whose K/V
+    are the oracle's per-chunk projections (project_chunk: norm + 3D RoPE at
+    each chunk's own positions), rounded to bf16 and appended; then recache
+    the present chunks {0, 4, 5, 6} from the same hidden states with the K|V
+    columns of the same weight.  Both the appended cache and the recached one
+    match the oracle model within the bf16 tolerance (H*D = 512: the K row
+    spans two GEMM tiles; 180-token chunks straddle row tiles)."""
+    sh = Shapes(4, 128, 60, 3, 3, 6, 10)
+    HD, Tc = sh.model_dim, sh.chunk_tokens
+    rng = np.random.default_rng(61)
+    w_qkv = torch.from_numpy((rng.standard_normal((HD, 3 * HD)) * 0.02).astype(np.float32)).to(torch.bfloat16)
+    gk = torch.from_numpy(rng.uniform(0.5, 1.5, HD).astype(np.float32))
+    w64 = bf16_to_f64(w_qkv)
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, sh.window_chunks)
+    model = CacheModel(sh.heads, sh.head_dim, Tc, sh.window_chunks)
+    hid = {}
+    for c in range(7):
+        hid[c] = torch.from_numpy(rng.standard_normal((Tc, HD)).astype(np.float32)).to(torch.bfloat16)
+        if c > sh.window_chunks:
+            cache.evict(c - sh.window_chunks)
+            model.evict(c - sh.window_chunks)
+        _, k, v = orc.project_chunk(bf16_to_f64(hid[c]), w64, None, gk.double().numpy(), c,
+                                    sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                                    sh.grid_w)
+        cache.append(torch.from_numpy(k).to(torch.bfloat16).cuda(),
+                     torch.from_numpy(v).to(torch.bfloat16).cuda(), c)
+        model.append(c, k, v)
+    ids = model.present_chunks()
+    assert ids == [0, 4, 5, 6]
+    torch.cuda.synchronize()
+    _compare_cache(cache, model, sh, what="appended")
+    hcat = torch.cat([hid[c] for c in ids]).cuda()
+    cache.recache(hcat, w_qkv[:, HD:].contiguous().cuda(), gk.cuda(), ids, sh.grid_h, sh.grid_w)
+    torch.cuda.synchronize()
+    _compare_cache(cache, model, sh, what="recached")
+    assert cache.last_device_error() == swl.KVC_OK
+
+
 def test_recache_rejections(swl):
     sh = TINY
     cache, model = _fill(swl, sh, 2)

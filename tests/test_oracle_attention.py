@@ -261,3 +261,16 @@ def test_attention_rows_against_brute_force_and_full_attention():
         got = oatt.attention_rows(q, k, v, 1.0 / math.sqrt(sh.head_dim), rows, heads)
         want = full[rows] if heads is None else full[rows][:, heads]
         assert np.allclose(got, want, rtol=0, atol=1e-13)
+
+
+def test_pool_matches_single_process():
+    """oracle.pool spreads attention_rows over spawned processes; the result
+    equals one call up to the library matmul's summation order."""
+    from oracle.pool import attention_rows_parallel
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((50, 3, 16))
+    k = rng.standard_normal((70, 3, 16))
+    v = rng.standard_normal((70, 3, 16))
+    rows = [49, 3, 17, 0, 25]
+    got = attention_rows_parallel(q, k, v, 0.3, rows, workers=2, rows_per_unit=2)
+    assert np.allclose(got, oatt.attention_rows(q, k, v, 0.3, rows), rtol=0, atol=1e-14)

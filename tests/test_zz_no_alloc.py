@@ -4,9 +4,9 @@ Some callers of this library cannot hand it device memory at call time -- their
 device memory is owned by another allocator, or their loop may not call
 cudaMalloc (it can synchronise the device).  kvc_quant_fp4_noalloc serves them:
 it takes the encoder's scratch from a static array inside the library instead
-of a caller buffer.  This test calls it through the C ABI twice in a row, on
-different inputs (so the second call starts from whatever the first left in
-the shared array), and checks that codes, block scales and tensor scale are
+of a caller buffer.  This test calls it through the C ABI three times in a row,
+on different inputs (each call starts from whatever the previous one left in
+the shared array, and the second one uses fewer of its words), and checks that codes, block scales and tensor scale are
 bit-identical to kvc_quant_fp4's on the same inputs -- the bar every FP4 encode
 test in this suite uses.  It lives in its own file, collected last, and passes
 both alone in a fresh process and after the rest of the suite.
@@ -45,10 +45,14 @@ def test_noalloc_matches_kvc_quant_fp4_twice(lib):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     ws = torch.empty(256, dtype=torch.int32, device=dev)  # scratch of the existing entry point
-    # two calls in a row: a LongLive-1.3B K chunk with outliers, then a smaller,
-    # ragged tensor with a much smaller tensor amax
+    # calls in a row on the shared array: a LongLive-1.3B K chunk with outliers
+    # (its first pass fills all 256 partial maxima), then a tensor of 800
+    # elements whose first pass writes only 100 partials and whose amax is
+    # about 1000x smaller -- a read of any word the previous call left would
+    # change its tensor scale -- then a ragged mid-size tensor
     inputs = [gaussian_outliers_bf16((4680, 12, 128), 0.01, 8.0, 77, 0, 0, 3),
-              gaussian_outliers_bf16((16 * 30001,), 0.01, 8.0, 77, 0, 1, 3) * 1e-3]
+              gaussian_outliers_bf16((16 * 50,), 0.01, 8.0, 77, 0, 2, 3) * 1e-3,
+              gaussian_outliers_bf16((16 * 30001,), 0.01, 8.0, 77, 0, 1, 3) * 1e-2]
     for i, x_cpu in enumerate(inputs):
         x = x_cpu.to(dev).contiguous()
         n = x.numel()
