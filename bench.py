@@ -1,13 +1,16 @@
 """Benchmark of the sink + short-window KV-cache hot path on one or more GPUs.
 
-One step = one pass over every operation of the path for one layer of the
-LongLive-1.3B-shaped workload (12 heads x 128, 4680-token chunks of 3 frames,
-sink + 3-slot window = 18720 cached tokens):
+The metric is the chunk attention of the LongLive-1.3B-shaped layer (12 heads
+x 128, a 4680-query chunk of 3 frames against 18720 cached keys: 1 sink chunk +
+3 window slots): TFLOP/s, latent frames/s per layer and % of the bf16 dense
+peak.  It is measured inside one step of the whole path:
     recache   [K|V] = Hid(18720x1536) @ W_kv(1536x3072), RMSNorm + 3D RoPE -> cache
     bf16      evict oldest chunk, append the new chunk, attention of its 4680 queries
     fp4       evict, append (FP4 encode), attention with fused dequantisation
 Steps rotate over 8 independent layer caches, so every step touches > 126 MB
-(larger than L2) that the previous step did not.
+(larger than L2) that the previous step did not.  A second leg streams 30
+layer caches x 320 chunks (evict + append + attention per layer and chunk) and
+reports the steady-state latent frames/s per layer.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 With N > 1 launch under torchrun: every rank runs its own replica (weak scaling).
@@ -128,61 +131,43 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU baseline: the float64 oracle on a bounded sample of the same step
+# CPU baseline: the float64 oracle on all host cores, on a sample of the
+# metric's own workload (query rows of the LongLive-1.3B layer attention)
 # ---------------------------------------------------------------------------
-def cpu_sample(frac_rows: int, seed: int = 0):
-    """Run the oracle on `frac_rows` query rows of both attentions, the same
-    share of the recache rows and of the FP4 encode; returns (seconds, flop)."""
+def cpu_attention_sample(rows: int, seed: int = 0):
+    """The oracle's attention (oracle.pool: attention_rows on a spawn pool over
+    every host core) for `rows` query rows x 12 heads against 18720 keys.
+    Returns (seconds, flop, worker processes); the seconds include the pool's
+    start-up (about a second)."""
     import numpy as np
-    from oracle import attention as oatt
-    from oracle import fp4 as ofp4
-    from oracle import recache as orc
+    from oracle.pool import attention_rows_parallel, host_cores
     rng = np.random.default_rng(seed)
     f32 = np.float32
     k = (rng.standard_normal((LK, H, D), dtype=f32) / math.sqrt(D)).astype(np.float64)
     v = rng.standard_normal((LK, H, D), dtype=f32).astype(np.float64)
-    q = (rng.standard_normal((frac_rows, H, D), dtype=f32) / math.sqrt(D)).astype(np.float64)
-    hid = rng.standard_normal((4 * frac_rows, HD), dtype=f32).astype(np.float64)
-    wkv = (rng.standard_normal((HD, 2 * HD), dtype=f32) * 0.02).astype(np.float64)
-    kq = rng.standard_normal((frac_rows, H, D), dtype=f32)
-    rows = np.arange(frac_rows)
+    q = (rng.standard_normal((rows, H, D), dtype=f32) / math.sqrt(D)).astype(np.float64)
+    cores = host_cores()
+    # one unit per (head, block of at most 1170 rows), at least as many units as cores
+    per = max(1, min(rows, 1170, -(-rows * H // cores)))
     t0 = time.perf_counter()
-    oatt.attention_rows(q, k, v, 1 / math.sqrt(D), rows)                     # bf16 row
-    ofp4.quantize(kq), ofp4.quantize(kq)                                       # FP4 encode share
-    oatt.attention_rows(q, k, v, 1 / math.sqrt(D), rows)                     # FP4 row (dequantised)
-    kk, vv = orc.project(hid, wkv)                                            # recache share
-    kk = orc.rmsnorm(kk, None, 1e-6).reshape(-1, H, D)
-    t = np.arange(kk.shape[0]) % TC
-    orc.rope3d(kk, t // TPF, (t % TPF) // GRID_W, t % GRID_W)
+    attention_rows_parallel(q, k, v, 1 / math.sqrt(D), rows_per_unit=per)
     dt = time.perf_counter() - t0
-    frac = frac_rows / TC
-    return dt, STEP_FLOP * frac
+    return dt, 4.0 * H * rows * LK * D, min(cores, H * -(-rows // per))
 
 
-def _blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
-        return 1
+def _sample_rows(target_s: float) -> int:
+    dt, _, _ = cpu_attention_sample(120)
+    return int(max(120, min(TC, 120 * target_s / max(dt, 1e-3))))
 
 
-def _cores():
-    """Threads the oracle runs on: its matmuls use the BLAS pool, the einsum
-    and elementwise parts one thread."""
-    return min(len(os.sched_getaffinity(0)), _blas_threads())
-
-
-def cpu_baseline(target_s: float = 12.0):
-    dt, _ = cpu_sample(8)
-    rows = int(max(8, min(TC, 8 * target_s / max(dt, 1e-3))))
-    dt, flop = cpu_sample(rows, seed=1)
-    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
-            "host_cpus": len(os.sched_getaffinity(0)), "blas_threads": _blas_threads(),
-            "sample": f"{rows} of 4680 query rows of both attentions (18720 keys, 12 heads), "
-                      f"{4 * rows} of 18720 recache rows, FP4 encode of {rows} rows; "
-                      f"{dt:.1f} s float64 numpy"}
+def cpu_baseline(target_s: float = 15.0):
+    rows = _sample_rows(target_s / 2)
+    dt, flop, cores = cpu_attention_sample(rows, seed=1)
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "host_cpus": len(os.sched_getaffinity(0)), "blas_threads_per_worker": 1,
+            "sample": f"{rows} of the 4680 query rows x 12 heads of the bf16 chunk attention "
+                      f"against 18720 keys ({rows / TC:.1%} of one call), float64 numpy on "
+                      f"{cores} spawned processes, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -191,24 +176,23 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    dt, _ = cpu_sample(8)
-    rows = int(max(8, min(TC, 8 * 4.0 / max(dt, 1e-3))))  # ~4 s per step
+    rows = _sample_rows(6.0)  # ~6 s per step
     for i in range(args.warmup):
-        cpu_sample(rows, seed=100 + i)
-    times, flop = [], 0.0
+        cpu_attention_sample(rows, seed=100 + i)
+    times, flop, cores = [], 0.0, 1
     for i in range(args.steps):
-        dt, flop = cpu_sample(rows, seed=1000 + i)
+        dt, flop, cores = cpu_attention_sample(rows, seed=1000 + i)
         times.append(dt)
     mean = sum(times) / len(times)
     value = flop / mean / 1e12
-    cores = _cores()
-    sample = (f"{rows} of 4680 query rows of both attentions, {4 * rows} recache rows, "
-              f"FP4 encode of {rows} rows per step")
+    sample = (f"{rows} of the 4680 query rows x 12 heads of the bf16 chunk attention against "
+              f"18720 keys per step, float64 numpy on {cores} spawned processes")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "latent_frames_per_s_per_layer": CF * (rows / TC) / mean,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -305,6 +289,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rolling", action="store_true",
+                    help="skip the 30-layer x 320-chunk rolling-stream leg")
     ap.add_argument("--layers", type=int, default=NLAYERS,
                     help="independent layer caches the steps rotate over (fewer: smaller "
                          "device footprint, e.g. for profiler captures)")
@@ -424,24 +410,24 @@ def main():
         total_ms += ev[s][0].elapsed_time(ev[s][-1])
         for i, r in enumerate(ROWS):
             row_ms[r] += ev[s][i].elapsed_time(ev[s][i + 1])
-    total_ms = max_over_ranks(total_ms, dist, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_tflops(STEP_FLOP, world, ms_per_step)
+    ms_per_step = max_over_ranks(total_ms / args.steps, dist, dev)
+    # the metric: the bf16 chunk attention of the LongLive-1.3B layer, timed
+    # inside each step (CUDA events on the launching stream around the call)
+    attn_ms = max_over_ranks(row_ms["attn_bf16"] / args.steps, dist, dev)
+    value = job_tflops(ATTN_FLOP, world, attn_ms)
 
-    # ---- end to end through the public API with host buffers.  Every step's
-    # inputs come from pinned host memory and its two attention outputs go back
-    # to it, all inside the timed region; the copies run on their own streams so
-    # that step s+1's inputs stream in (and step s-1's outputs stream out)
-    # while step s computes, and the host reads step s-1's result meanwhile.
-    host = {n: layers[0][n].cpu().pin_memory() for n in ("q", "k", "v", "k4", "v4", "hid")}
-    host["wkv"] = wkv.cpu().pin_memory()
-    out_h = [[torch.empty((TC, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-             for _ in range(2)]
+    # ---- end to end through the public API with host buffers: the same chunk
+    # attention, with every step's Q, K and V copied in from pinned host memory
+    # (evict + append + attention on a bf16 cache) and its output copied back,
+    # all inside the timed region.  The copies run on their own streams: step
+    # s+1's inputs stream in and step s-1's output streams out while step s
+    # computes, and the host reads step s-1's result meanwhile.  (The FP4
+    # caches are not used after this point.)
+    host = {n: layers[0][n].cpu().pin_memory() for n in ("q", "k", "v")}
+    out_h = [torch.empty((TC, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_h[0])
-    n_e2e = max(3, min(args.steps, 10))
-    for L in layers:  # per-layer weight buffer: a copy never races a recache reading it
-        L["wkv"] = torch.empty_like(wkv)
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    n_e2e = max(3, min(2 * args.steps, 24))
     comp = torch.cuda.current_stream()
     cs, ds = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     copied = [torch.cuda.Event() for _ in range(n_e2e)]
@@ -454,9 +440,16 @@ def main():
         with torch.cuda.stream(cs):
             if s >= nlayers:  # the layer's buffers are free once step s - nlayers is done
                 cs.wait_event(done[s - nlayers])
-            for n in ("q", "k", "v", "k4", "v4", "hid", "wkv"):
+            for n in ("q", "k", "v"):
                 L[n].copy_(host[n], non_blocking=True)
             copied[s].record(cs)
+
+    def chunk_step(L):
+        c = L["c"] + 1
+        L["bf"].evict(c - W)
+        L["bf"].append(L["k"], L["v"], c)
+        L["bf"].attn(L["q"], scale, out=L["o"])
+        L["c"] = c
 
     if dist:
         dist.barrier()
@@ -469,14 +462,13 @@ def main():
         if s + 1 < n_e2e:
             enqueue_inputs(s + 1)
         comp.wait_event(copied[s])
-        if s >= nlayers:  # the layer's outputs of step s - nlayers have been read back
-            comp.wait_event(fetched[s - nlayers])
-        step(L, wkv_t=L["wkv"])
+        if s >= 2:  # the output buffer of step s - 2 has been read back
+            comp.wait_event(fetched[s - 2])
+        chunk_step(L)
         done[s].record(comp)
         with torch.cuda.stream(ds):
             ds.wait_event(done[s])
-            out_h[s % 2][0].copy_(L["o"], non_blocking=True)
-            out_h[s % 2][1].copy_(L["o4"], non_blocking=True)
+            out_h[s % 2].copy_(L["o"], non_blocking=True)
             fetched[s].record(ds)
         if s >= 1:
             fetched[s - 1].synchronize()  # the host reads step s-1's result
@@ -484,17 +476,19 @@ def main():
     comp.wait_event(fetched[n_e2e - 1])
     e_end.record(comp)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end) / n_e2e
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    e2e_value = job_tflops(STEP_FLOP, world, e2e_ms)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / n_e2e, dist, dev)
+    e2e_value = job_tflops(ATTN_FLOP, world, e2e_ms)
 
     hbm = hbm_kernels(swl, dev, layers, randn)
-
     for L in layers:
         for cache in (L["bf"], L["f4"]):
             st = cache.last_device_error()
             if st != swl.KVC_OK:
                 raise RuntimeError(f"device error after the bench: {swl.status_string(st)}")
+    del layers, host
+    torch.cuda.empty_cache()
+
+    rolling = None if args.no_rolling else rolling_stream(swl, dev, rank, dist)
 
     if rank != 0:
         if dist:
@@ -511,10 +505,11 @@ def main():
               "attn_bf16": ATTN_BF16_BYTES, "attn_fp4": ATTN_FP4_BYTES, "recache": RECACHE_BYTES}
     rows = {}
     for r in ROWS:
-        d = {"ms": per[r], "share": per[r] / ms_per_step}
+        d = {"ms": per[r], "share": per[r] / (total_ms / steps)}
         if r in flops and per[r] > 0:
             d["tflops"] = flops[r] / (per[r] * 1e-3) / 1e12
             d["frac_bf16_peak"] = d["tflops"] / peak
+            d["frac_bf16_peak_sustained"] = d["tflops"] / peak_sus
         if r in bytes_ and per[r] > 0:
             d["gbs"] = bytes_[r] / (per[r] * 1e-3) / 1e9
             if r.startswith("append"):
@@ -530,19 +525,26 @@ def main():
     tr = TRAFFIC.get(kname)
     traffic = tr["bytes"] if tr and tr["src_sha"] == _src_sha(src) else None
     achieved = flops[dom] / (per[dom] * 1e-3) / 1e12
-    chunk_step_ms = per["evict_bf16"] + per["append_bf16"] + per["attn_bf16"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step": "recache + (evict, append, attention) on a bf16 "
-                   "cache + (evict, FP4 append, attention) on an FP4 cache",
+        "config": {"workload": WORKLOAD,
+                   "value": "bf16 chunk attention, 4680 queries x 18720 keys x 12 heads x 128 "
+                            f"({ATTN_FLOP / 1e9:.2f} GFLOP per call), CUDA events around the call "
+                            "inside each step, all ranks' calls over the slowest rank's time",
+                   "step": "recache + (evict, append, attention) on a bf16 cache + (evict, FP4 "
+                           "append, attention) on an FP4 cache",
                    "step_gflop": STEP_FLOP / 1e9, "layers_rotated": nlayers,
                    "l2": f"inputs larger than L2: {nlayers} rotating layer caches, each step "
                          "touches > 200 MB (the L2 holds 126 MB)",
                    "prewarm_steps": prewarm,
                    "parallelism": f"replicas x{world}"},
-        "latent_frames_per_s_per_layer": CF / (chunk_step_ms * 1e-3),
+        "attn_ms": attn_ms,
+        "attn_frac_bf16_peak": value / world / peak,
+        "attn_frac_bf16_peak_sustained": value / world / peak_sus,
+        "latent_frames_per_s_per_layer": CF / (attn_ms * 1e-3),
+        "step_tflops": job_tflops(STEP_FLOP, world, ms_per_step),
         "rows": rows,
         "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
@@ -550,7 +552,10 @@ def main():
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
                      "traffic": traffic},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
+                "what": "per step: Q, K, V of one chunk host->device, evict + append + "
+                        "attention through the public API, O device->host"},
+        "rolling": rolling,
         "hbm_kernels": hbm,
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
@@ -561,6 +566,66 @@ def main():
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def rolling_stream(swl, dev, rank, dist, n_layers: int = 30, n_chunks: int = 320):
+    """The rolling stream: n_layers independent bf16 layer caches, n_chunks
+    chunks; for every chunk, every layer evicts its oldest window chunk (from
+    chunk W + 1 on), appends the new chunk and runs its attention, the sink
+    pinned.  Each chunk's Q/K/V for all layers are drawn on the device (seeded
+    per chunk) before that chunk's timed region; CUDA events bracket the
+    n_layers x (evict + append + attention) of a chunk.  Steady state: chunks
+    >= 4 (the window full and evicting)."""
+    import torch
+    caches = [swl.KVCache(H, D, TPF, CF, W, dtype="bf16", device=dev) for _ in range(n_layers)]
+    qkv = [[torch.empty((TC, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+           for _ in range(n_layers)]
+    out = torch.empty((TC, H, D), dtype=torch.bfloat16, device=dev)
+    g = torch.Generator(device=dev)
+    scale = 1.0 / math.sqrt(D)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_chunks)]
+    std = (1 / math.sqrt(D), 1 / math.sqrt(D), 1.0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for c in range(n_chunks):
+        g.manual_seed(100003 * (rank + 1) + c)
+        for li in range(n_layers):
+            for t, sd in zip(qkv[li], std):
+                t.copy_(torch.randn((TC, H, D), generator=g, device=dev) * sd)
+        evs[c][0].record()
+        for li in range(n_layers):
+            cache = caches[li]
+            if c > W:
+                cache.evict(c - W)
+            cache.append(qkv[li][1], qkv[li][2], c)
+            cache.attn(qkv[li][0], scale, out=out)
+        evs[c][1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    want = [0] + [-1] * W
+    for x in range(max(1, n_chunks - W), n_chunks):  # the last W chunks, slot (x - 1) mod W
+        want[1 + (x - 1) % W] = x
+    for cache in caches:
+        if cache.chunk_of_region != want:
+            raise RuntimeError(f"rolling stream: slot map {cache.chunk_of_region}, want {want}")
+        st = cache.last_device_error()
+        if st != swl.KVC_OK:
+            raise RuntimeError(f"device error in the rolling stream: {swl.status_string(st)}")
+    steady = [a.elapsed_time(b) for a, b in evs[4:]]
+    ms_chunk = max_over_ranks(sum(steady) / len(steady), dist, dev)
+    ms_layer = ms_chunk / n_layers
+    return {"layers": n_layers, "chunks": n_chunks, "steady_chunks": len(steady),
+            "latent_frames": n_chunks * CF,
+            "ms_per_layer_step": ms_layer,
+            "latent_frames_per_s_per_layer": CF / (ms_layer * 1e-3),
+            "latent_frames_per_s_all_layers": CF / (ms_chunk * 1e-3),
+            "attn_tflops": ATTN_FLOP / (ms_layer * 1e-3) / 1e12,
+            "wall_s": wall,
+            "timing": "CUDA events around each chunk's 30 x (evict + append + attention), "
+                      "chunks >= 4; wall_s includes drawing the inputs on the device"}
 
 
 if __name__ == "__main__":
