@@ -55,10 +55,13 @@ def rope_bands(head_dim: int):
 
 
 def token_positions(chunk_id: int, chunk_tokens: int, tokens_per_frame: int,
-                    chunk_frames: int, grid_w: int):
-    """(frame, h, w) integer positions of the tokens of one chunk, each [Tc]."""
+                    chunk_frames: int, grid_w: int, frame0: int | None = None):
+    """(frame, h, w) integer positions of the tokens of one chunk, each [Tc].
+    frame0: frame position of the chunk's first frame (default chunk_id *
+    chunk_frames; a multi-shot cache shifts it, see cache_model)."""
     t = np.arange(chunk_tokens)
-    f = chunk_id * chunk_frames + t // tokens_per_frame
+    f0 = chunk_id * chunk_frames if frame0 is None else frame0
+    f = f0 + t // tokens_per_frame
     p = t % tokens_per_frame
     return f, p // grid_w, p % grid_w
 
@@ -88,9 +91,10 @@ def rope3d(x: np.ndarray, pos_f, pos_h, pos_w, theta: float = 10000.0) -> np.nda
 
 def recache(hidden, w_kv, gamma, chunk_ids, heads: int, head_dim: int,
             tokens_per_frame: int, chunk_frames: int, grid_w: int,
-            eps: float = 1e-6, theta: float = 10000.0):
+            eps: float = 1e-6, theta: float = 10000.0, frame0=None):
     """K, V [n*Tc][H][D] float64 for hidden rows of the chunks in ``chunk_ids``
-    (logical order, sink first)."""
+    (logical order, sink first).  frame0: per chunk, the frame position of its
+    first frame (default chunk_id * chunk_frames)."""
     k, v = project(hidden, w_kv)
     k = rmsnorm(k, gamma, eps)
     T = k.shape[0]
@@ -100,8 +104,9 @@ def recache(hidden, w_kv, gamma, chunk_ids, heads: int, head_dim: int,
     k = k.reshape(T, heads, head_dim)
     v = v.reshape(T, heads, head_dim)
     pf, ph, pw = [], [], []
-    for c in chunk_ids:
-        f, h, w = token_positions(c, Tc, tokens_per_frame, chunk_frames, grid_w)
+    for i, c in enumerate(chunk_ids):
+        f, h, w = token_positions(c, Tc, tokens_per_frame, chunk_frames, grid_w,
+                                  None if frame0 is None else frame0[i])
         pf.append(f), ph.append(h), pw.append(w)
     k = rope3d(k, np.concatenate(pf), np.concatenate(ph), np.concatenate(pw), theta)
     return k, v
@@ -109,7 +114,7 @@ def recache(hidden, w_kv, gamma, chunk_ids, heads: int, head_dim: int,
 
 def project_chunk(hidden, w_qkv, gamma_q, gamma_k, chunk_id: int, heads: int, head_dim: int,
                   tokens_per_frame: int, chunk_frames: int, grid_w: int,
-                  eps: float = 1e-6, theta: float = 10000.0):
+                  eps: float = 1e-6, theta: float = 10000.0, frame0: int | None = None):
     """Q, K, V [Tc][H][D] float64 of ONE new chunk, as the layer produces them
     before they are attended to and appended.
 
@@ -125,7 +130,7 @@ def project_chunk(hidden, w_qkv, gamma_q, gamma_k, chunk_id: int, heads: int, he
     x = np.asarray(hidden, dtype=np.float64) @ np.asarray(w_qkv, dtype=np.float64)
     hd = heads * head_dim
     Tc = x.shape[0]
-    f, h, w = token_positions(chunk_id, Tc, tokens_per_frame, chunk_frames, grid_w)
+    f, h, w = token_positions(chunk_id, Tc, tokens_per_frame, chunk_frames, grid_w, frame0)
     q = rope3d(rmsnorm(x[:, :hd], gamma_q, eps).reshape(Tc, heads, head_dim), f, h, w, theta)
     k = rope3d(rmsnorm(x[:, hd:2 * hd], gamma_k, eps).reshape(Tc, heads, head_dim), f, h, w, theta)
     v = x[:, 2 * hd:].reshape(Tc, heads, head_dim)

@@ -274,3 +274,107 @@ def test_pool_matches_single_process():
     rows = [49, 3, 17, 0, 25]
     got = attention_rows_parallel(q, k, v, 0.3, rows, workers=2, rows_per_unit=2)
     assert np.allclose(got, oatt.attention_rows(q, k, v, 0.3, rows), rtol=0, atol=1e-14)
+
+
+def _shot_stream(m, n_chunks, shots, k_of, v_of):
+    """Stream chunks 0..n_chunks-1 through a CacheModel; chunks in `shots` open
+    a new shot.  Step c evicts c - W when it is in the window."""
+    for c in range(n_chunks):
+        if (c - m.W) in m.window_chunks():
+            m.evict(c - m.W)
+        (m.append_shot if c in shots else m.append)(c, k_of(c), v_of(c))
+        yield c
+
+
+def test_multi_shot_sink_state_and_positions():
+    """Multi-shot sink: the first chunk of a new shot becomes the sink and the
+    old sink leaves; the window keeps the previous shot's recent chunks; the
+    new sink's own ring slot stays unused; positions shift by the RoPE offset
+    at every boundary after chunk 0."""
+    W, Tc, cf, off = 2, 2, 3, 7
+    m = CacheModel(1, 16, Tc, W, chunk_frames=cf, rope_offset_frames=off)
+    z = lambda c: np.full((Tc, 1, 16), float(c))
+    seen = {}
+    for c in _shot_stream(m, 9, {0, 5}, z, z):
+        seen[c] = (list(m.chunk_of_region), m.present_chunks(), m.frame0_of_region())
+    assert seen[4][0] == [0, 3, 4]
+    assert seen[5][0] == [5, -1, 4]           # 3 evicted, 5 is the sink, 0 gone
+    assert seen[5][1] == [5, 4]
+    assert seen[6][0] == [5, -1, 6]           # 4 evicted; 6 in slot (6-1) % 2
+    assert seen[7][0] == [5, 7, 6]            # 5 is the sink, not evicted; 7 in 5's old slot
+    assert seen[8][0] == [5, 7, 8]
+    assert seen[4][2] == [0, 9, 12]           # frame0 = c*cf before the boundary
+    assert seen[8][2] == [5 * cf + off, 7 * cf + off, 8 * cf + off]
+    with pytest.raises(CacheStateError):
+        m.evict(5)                            # the shot's sink is never evicted
+    with pytest.raises(CacheStateError):
+        m.append_shot(7, z(7), z(7))          # a shot starts at the next chunk only
+    m.append_shot(9, z(9), z(9))
+    assert m.chunk_of_region[0] == 9 and m.shot == 2 and m.frame0[9] == 9 * cf + 2 * off
+    m.append_shot(9, z(9), z(9))              # overwrite of the shot's own sink
+    assert m.shot == 2
+    m.append(9, z(9), z(9))                   # the same through the plain append
+    assert m.chunk_of_region[0] == 9
+
+
+def _masked_full(q_all, k_all, v_all, Tc, visible, scale):
+    """Masked softmax over the whole sequence: query chunk i sees key chunk j iff
+    visible(i, j)."""
+    T, H, D = q_all.shape
+    ci = np.arange(T) // Tc
+    n = T // Tc
+    vis = np.array([[visible(i, j) for j in range(n)] for i in range(n)])
+    mask = vis[ci][:, ci]
+    out = np.empty_like(q_all)
+    for h in range(H):
+        s = (q_all[:, h, :] @ k_all[:, h, :].T) * scale
+        s = np.where(mask, s, -np.inf)
+        s -= s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ v_all[:, h, :]
+    return out
+
+
+def test_multi_shot_window_covering_all_equals_masked_full_attention():
+    """With a window wider than the stream, a multi-shot cache shows query
+    chunk i every key chunk j <= i except the sinks of earlier shots: the
+    oracle's step outputs equal one masked softmax over the whole sequence."""
+    sh = TINY
+    n, shots = 7, {0, 3, 5}
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    m = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, window_chunks=n)
+    data = {c: tuple(bf16_to_f64(t) for t in chunk_qkv(sh, 0, 0, c, "rms1")) for c in range(n)}
+    outs = []
+    for c in _shot_stream(m, n, shots, lambda c: data[c][1], lambda c: data[c][2]):
+        outs.append(oatt.sinkwin_attention(m, data[c][0], scale))
+    starts = sorted(shots)
+
+    def visible(i, j):
+        cur = max(s for s in starts if s <= i)
+        return j <= i and (j not in starts or j == cur)
+
+    full = _masked_full(*(np.concatenate([data[c][t] for c in range(n)]) for t in range(3)),
+                        sh.chunk_tokens, visible, scale)
+    assert np.allclose(np.concatenate(outs), full, rtol=0, atol=1e-12)
+
+
+def test_multi_shot_old_sink_has_no_influence_new_sink_always_does():
+    sh = TINY
+    scale = 0.125
+    W = sh.window_chunks
+    rng = np.random.default_rng(21)
+    data = {c: tuple(bf16_to_f64(t) for t in chunk_qkv(sh, 0, 1, c, "rms1")) for c in range(8)}
+    bump = lambda c, which, d: data[c][which] + (d if c == which_chunk[0] else 0.0)
+    outs = {}
+    for variant, which_chunk in (("base", [-1]), ("old", [0]), ("new", [4])):
+        m = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, W)
+        res = []
+        for c in _shot_stream(m, 8, {0, 4}, lambda c: bump(c, 1, 3.0), lambda c: bump(c, 2, -2.0)):
+            res.append(oatt.sinkwin_attention(m, data[c][0], scale))
+        outs[variant] = res
+    for c in range(4, 8):
+        assert np.array_equal(outs["base"][c], outs["old"][c])  # old sink gone: bit-identical
+        assert np.max(np.abs(outs["base"][c] - outs["new"][c])) > 1e-3  # new sink counts
+    assert np.max(np.abs(outs["base"][2] - outs["old"][2])) > 1e-3
+    del rng

@@ -132,3 +132,38 @@ def test_recache_equals_appended_chunk_projections():
     qq, _ = orc.recache(hid[6], np.concatenate([w_qkv[:, :HD], w_qkv[:, :HD]], axis=1), gq, [6],
                         H, D, tpf, cf, gw)
     assert np.allclose(q, qq, rtol=0, atol=1e-12)
+
+
+def test_recache_with_shot_offsets_equals_appended_projections():
+    """Multi-shot positions: chunks projected at frame0 = c*cf + shot*offset
+    and appended (a shot boundary at chunk 5) are reproduced by a recache that
+    takes each region's frame0 from the cache model."""
+    from oracle.cache_model import CacheModel
+    rng = np.random.default_rng(6)
+    H, D, tpf, cf, gw, W, off = 2, 64, 16, 2, 4, 2, 11
+    Tc, HD = tpf * cf, H * D
+    w_qkv = rng.standard_normal((HD, 3 * HD)) * 0.05
+    gk = rng.uniform(0.5, 1.5, HD)
+    m = CacheModel(H, D, Tc, W, chunk_frames=cf, rope_offset_frames=off)
+    hid = {}
+    for c in range(7):
+        hid[c] = rng.standard_normal((Tc, HD))
+        if (c - W) in m.window_chunks():
+            m.evict(c - W)
+        shot = c == 5
+        f0 = c * cf + (m.shot + (1 if shot else 0)) * off
+        _, k, v = orc.project_chunk(hid[c], w_qkv, None, gk, c, H, D, tpf, cf, gw, frame0=f0)
+        (m.append_shot if shot else m.append)(c, k, v)
+        assert m.frame0[c] == f0
+    ids = m.present_chunks()
+    assert ids == [5, 6] and m.chunk_of_region == [5, -1, 6]
+    K0, V0 = m.physical(fill=0.0)
+    k, v = orc.recache(np.concatenate([hid[c] for c in ids]), w_qkv[:, HD:], gk, ids, H, D, tpf,
+                       cf, gw, frame0=[m.frame0[c] for c in ids])
+    m.recache(ids, k, v)
+    K1, V1 = m.physical(fill=0.0)
+    assert np.allclose(K1, K0, rtol=0, atol=1e-12) and np.allclose(V1, V0, rtol=0, atol=1e-12)
+    # the offset matters: absolute positions give different keys
+    k_abs, _ = orc.recache(np.concatenate([hid[c] for c in ids]), w_qkv[:, HD:], gk, ids, H, D,
+                           tpf, cf, gw)
+    assert np.max(np.abs(k_abs - k)) > 1e-3
