@@ -12,15 +12,22 @@
  * blog.hotdry.top, "NVFP4 量化与 KV Cache 压缩的工程实现": inference.kv_quant).
  *
  * Layout.  One layer's cache has (1 + W) regions of Tc = chunk_frames *
- * tokens_per_frame rows each.  Region 0 holds the sink (chunk 0); chunk c >= 1
- * lives in region 1 + (c - 1) % W.  Row r of region g is physical row
- * g * Tc + r of
+ * tokens_per_frame rows each.  Region 0 holds the sink (chunk 0, or the first
+ * chunk of the current shot after kvc_append_shot); a window chunk c >= 1 lives
+ * in region 1 + (c - 1) % W.  Row r of region g is physical row g * Tc + r of
  *     bf16 cache:  k, v            bf16  [S][H][D]          S = (1 + W) * Tc
  *     FP4 cache:   k, v            uint8 [S][H][D/2]        E2M1 codes, element 2i in
  *                                                           the low nibble
  *                  k_scale,v_scale uint8 [S][H][D/16]       E4M3 scale per 16 elements
  *                  k_gscale,...    float [1 + W]            fp32 tensor scale per region
  * Decoded value: e2m1(code) * e4m3(scale) * gscale[region].
+ *
+ * RoPE positions.  Token t of chunk c sits at frame frame0(c) + t / tokens_per_frame,
+ * patch row (t % tokens_per_frame) / grid_w, column t % grid_w, with
+ * frame0(c) = c * chunk_frames + shot(c) * rope_offset_frames, shot(c) being the
+ * number of shot boundaries (kvc_append_shot of a chunk > 0) at or before c.  Keys
+ * handed to kvc_append are expected to carry these positions; kvc_recache and
+ * kvc_project_append apply them.
  *
  * Conventions.
  *  - All device memory (cache, inputs, outputs, workspace) is allocated by the
@@ -91,11 +98,24 @@ typedef struct kvc_cache {
                         CTA boundary are merged through it); without it every CTA
                         takes whole items.  Calls sharing it must be stream-ordered. */
   uint64_t attn_ws_bytes; /* its size in bytes */
+  void* stage;       /* optional staging buffer (16-byte aligned) of up to
+                        kvc_cache_bytes(c, 8) bytes, or NULL: fp32 rows waiting for
+                        their RMSNorm, and bf16 K/V waiting for their FP4 encode.
+                        Needed by kvc_recache on an FP4 cache and by kvc_project_append
+                        (each states how much it uses).  Contents need no init;
+                        calls sharing it must be stream-ordered. */
+  uint64_t stage_bytes; /* its size in bytes */
   /* ---- options ---- */
-  int32_t scrub_on_evict; /* nonzero: kvc_evict overwrites the freed slot with NaN */
+  int32_t scrub_on_evict;     /* nonzero: kvc_evict overwrites the freed slot with NaN */
+  int32_t rope_offset_frames; /* multi-shot RoPE offset: each shot boundary (kvc_append_shot)
+                                 shifts the frame positions of that chunk and every later
+                                 one by this many frames (0: positions stay absolute) */
   /* ---- library-maintained state: read-only for the caller ---- */
   int32_t init_magic;
-  int64_t chunk_of_region[1 + KVC_MAX_WINDOW]; /* -1 = empty */
+  int32_t shot;                                /* shot boundaries so far */
+  int64_t chunk_of_region[1 + KVC_MAX_WINDOW]; /* -1 = empty; region 0 = the sink */
+  int64_t frame0_of_region[1 + KVC_MAX_WINDOW]; /* RoPE frame position of the first frame
+                                                   of the chunk each region holds; -1 = empty */
   int64_t last_chunk;                          /* highest chunk appended so far, -1 = none */
 } kvc_cache;
 
@@ -104,8 +124,11 @@ size_t kvc_sizeof_cache(void);
 
 /* Bytes of one device buffer of a cache with this geometry.
  * which: 0 k, 1 v, 2 k_scale, 3 v_scale, 4 k_gscale, 5 v_gscale, 6 dev_ws,
- * 7 attn_ws (depends on the SM count of the current device; 0 without one).
- * Returns 0 for a buffer the dtype does not use or for an invalid geometry. */
+ * 7 attn_ws (depends on the SM count of the current device; 0 without one),
+ * 8 stage (the most any call uses: Tc * H*D * 4 * max(1 + W, 3)).
+ * Returns 0 for a buffer the dtype does not use or for an invalid geometry.
+ * Cache = sink + W window slots: LongLive summary page, 方法 §3 高效长推理 (帧汇聚点,
+ * 短窗口注意力: the per-layer cache size depends on the window only). */
 size_t kvc_cache_bytes(const kvc_cache* c, int32_t which);
 
 /* Validate geometry and buffers, mark every region empty.  No GPU work.
@@ -117,16 +140,35 @@ int32_t kvc_init(kvc_cache* c);
  * chunk c >= 1 goes to ring slot (c-1) % W.  Allowed: chunk 0 into an empty
  * cache; the last appended chunk again while it is still cached (overwrite, one
  * call per denoise step); chunk last_chunk + 1 once its slot is empty (evict the
- * oldest window chunk first).  Else KVC_ESTATE.  bf16 cache: a 128-bit vectorised copy.  FP4 cache: the chunk's K
- * and V are quantised (tensor amax -> fp32 gscale[region], E4M3 block scales,
- * E2M1 codes; the encode rule is kvc_quant_fp4's). */
+ * oldest window chunk first).  Else KVC_ESTATE.  bf16 cache: a 128-bit
+ * vectorised copy.  FP4 cache: the chunk's K and V are quantised (tensor amax ->
+ * fp32 gscale[region], E4M3 block scales, E2M1 codes; the encode rule is
+ * kvc_quant_fp4's).
+ * Defined by: LongLive summary page, 方法 §3 (each new chunk's keys/values join
+ * the window; the first chunk stays as the frame sink). */
 int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
                    kvc_stream_t stream);
+
+/* Append chunk `chunk_idx` as the first chunk of a new shot: it becomes the
+ * sink (region 0) and the previous sink leaves the cache; the window slots keep
+ * what they hold (the previous shot's recent chunks still give continuity) and
+ * later chunks fill the ring as usual (chunk_idx's own ring slot stays unused).
+ * Allowed: chunk last_chunk + 1 (or 0 into an empty cache), or the current sink
+ * again when it is the last chunk appended (overwrite); else KVC_ESTATE.  The
+ * shot count grows by one for chunk_idx > 0, which shifts RoPE positions by
+ * rope_offset_frames from this chunk on.  Arguments and encode as kvc_append.
+ * Defined by: LongLive 2.0 inference blog (blog.hotdry.top), "序列并行与注意力汇聚的
+ * 协同设计" (inference.multi_shot_sink resets the sink at each shot boundary;
+ * inference.multi_shot_rope_offset shifts the RoPE positions). */
+int32_t kvc_append_shot(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
+                        kvc_stream_t stream);
 
 /* Evict chunk `chunk_idx`, which must be the oldest window chunk (the sink is
  * never evicted: KVC_ESTATE).  Moves no data: the slot is marked empty.  With
  * scrub_on_evict set, the slot's rows are overwritten with NaN (bf16 0x7FC0;
- * FP4: codes 0, scales 0x7F) so a stale read would show. */
+ * FP4: codes 0, scales 0x7F) so a stale read would show.
+ * Defined by: LongLive summary page, 方法 §3 短窗口注意力 (attention covers only a
+ * fixed window of recent frames). */
 int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
 
 /* out = softmax(softmax_scale * q K^T) V per head, over the visible keys: the
@@ -135,12 +177,17 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
  * [tq][H][D]; tq >= 0 (0 is a no-op); softmax_scale finite and >= 0 (else
  * KVC_EINVAL).  D in {64, 128} (else KVC_EUNSUPPORTED); the sink must be
  * present (else KVC_ESTATE).  A kernel wait that runs out leaves KVC_ETIMEOUT
- * for kvc_last_device_error.
+ * for kvc_last_device_error.  Any tq runs on every SM: queries of a head are cut
+ * into 256-row items and items into pieces of K/V tiles when there are fewer
+ * items than SMs (pieces merged through attn_ws; without it whole items).
  * Arithmetic: bf16 operands, fp32 accumulation and softmax, bf16 output.  FP4
  * caches are dequantised inside the tile load, exactly: K as e2m1 * s (bf16),
  * V as e2m1 * s (f16); the regions' fp32 tensor scales enter the logit scale
  * (K) and P (V, P stored as f16 after dividing every V scale by one power of
- * two covering the largest, so any finite magnitude of V is representable). */
+ * two covering the largest, so any finite magnitude of V is representable).
+ * Defined by: LongLive summary page, 方法 §3 高效长推理 (queries attend to the
+ * frame-sink tokens joined with the short window); FP4 read: LongLive 2.0
+ * inference blog, "NVFP4 量化与 KV Cache 压缩的工程实现" (fused dequantisation). */
 int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
                      float softmax_scale, kvc_stream_t stream);
 
@@ -152,19 +199,42 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
  * hidden: device bf16 [n*Tc][H*D]; w_kv: device bf16 [H*D][2*H*D], the K columns
  * first; gamma_k: device fp32 [H*D], 16-byte aligned, or NULL (= ones); hidden and
  * w_kv 16-byte aligned (else KVC_EINVAL).  RMSNorm spans the whole
- * H*D-wide K row: x / sqrt(mean(x^2) + eps).  3D RoPE: token t of chunk c is at
- * frame c*chunk_frames + t / tokens_per_frame, row (t % tpf) / grid_w, column
- * t % grid_w (grid_h * grid_w == tokens_per_frame); the D/2 rotation pairs
- * (adjacent elements) are split into [frame | row | column] bands of
+ * H*D-wide K row: x / sqrt(mean(x^2) + eps).  3D RoPE at each chunk's positions
+ * (frame0_of_region of its region; see "RoPE positions" above); the D/2 rotation
+ * pairs (adjacent elements) are split into [frame | row | column] bands of
  * (P - 2*(P/3), P/3, P/3) pairs, P = D/2; in a band of b dims pair j turns by
- * position * rope_theta^(-2j/b).  bf16 caches only (FP4: KVC_EUNSUPPORTED);
+ * position * rope_theta^(-2j/b).  grid_h * grid_w == tokens_per_frame.
  * H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} (else KVC_EUNSUPPORTED).
- * Runs as three launches on `stream` (K projection, norm + RoPE, V projection);
- * between them the regions being rebuilt hold intermediate values, so nothing
- * may read those regions until the stream passes the call. */
+ * bf16 cache: three launches on `stream` (K projection, norm + RoPE, V
+ * projection); between them the regions being rebuilt hold intermediate values,
+ * so nothing may read those regions until the stream passes the call.
+ * FP4 cache: the same three launches write bf16 K and V of all n chunks into
+ * `stage` (n * Tc * H*D * 4 bytes needed, else KVC_EINVAL), then each region is
+ * FP4-encoded from them with kvc_quant_fp4's rule (its own tensor scale).
+ * Defined by: LongLive summary page, 方法 §1 KV 重缓存 (at the switch the cache is
+ * recomputed from the generated frames with the new prompt); FP4 store: LongLive
+ * 2.0 inference blog, "NVFP4 量化与 KV Cache 压缩的工程实现". */
 int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const float* gamma_k,
                     float eps, const int64_t* chunk_ids, int32_t n, int32_t grid_h,
                     int32_t grid_w, float rope_theta, kvc_stream_t stream);
+
+/* Project one new chunk and append its keys and values: 
+ *   [Q | K | V] = hidden @ w_qkv;  Q <- RoPE3D(RMSNorm(Q) * gamma_q);
+ *   K <- RoPE3D(RMSNorm(K) * gamma_k);  q_out <- Q;  K, V appended as chunk_idx
+ * (as kvc_append, or kvc_append_shot when new_shot is nonzero).  hidden: device
+ * bf16 [Tc][H*D]; w_qkv: device bf16 [H*D][3*H*D] (Q columns, then K, then V);
+ * gamma_q, gamma_k: device fp32 [H*D] or NULL (= ones); q_out: device bf16
+ * [Tc][H][D].  Norm, RoPE, eps, rope_theta, grid and the supported H*D as in
+ * kvc_recache; positions frame0(chunk_idx).  Uses `stage`: Tc * H*D * 8 bytes
+ * (bf16 cache) or 12 (FP4 cache), else KVC_EINVAL.  Two launches (the GEMM over
+ * all 3*H*D columns, then norm + RoPE of Q and K), plus the FP4 encode's two.
+ * Defined by: LongLive summary page, 方法 (causal frame-level autoregression: each
+ * chunk is projected and its keys/values join the cache every later chunk
+ * reads) and §3 帧汇聚点. */
+int32_t kvc_project_append(kvc_cache* c, const void* hidden, const void* w_qkv,
+                           const float* gamma_q, const float* gamma_k, float eps,
+                           int64_t chunk_idx, int32_t new_shot, int32_t grid_h, int32_t grid_w,
+                           float rope_theta, void* q_out, kvc_stream_t stream);
 
 /* FP4-encode n finite bf16 values (device x, n % 16 == 0, n >= 16; the codes of
  * a tensor holding NaN or infinity are unspecified) as one tensor:
@@ -175,7 +245,10 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
  * codes: device uint8 [n/2] (element 2i in the low nibble); scales: device uint8
  * [n/16]; gscale: device float [1]; ws: device scratch of KVC_QUANT_WS_WORDS
  * int32 words that the call overwrites (per-CTA partial maxima; calls that share
- * a ws must be stream-ordered).  n up to 2^31 * 16. */
+ * a ws must be stream-ordered).  n up to 2^31 * 16.
+ * Defined by: LongLive 2.0 inference blog, "NVFP4 量化与 KV Cache 压缩的工程实现"
+ * (inference.kv_quant: FP4 KV store); the format's rounding details are this
+ * library's reading (the page names only FP4/NVFP4). */
 int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, float* gscale,
                       int32_t* ws, kvc_stream_t stream);
 
@@ -187,11 +260,12 @@ int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
  * outputs as kvc_quant_fp4 minus `ws`; the library allocates nothing.
  * Scratch: a static device array of KVC_NOALLOC_SCRATCH_WORDS int32 (1 KiB)
  * inside the library, held by every GPU that loads it until the process exits.
- * Its device address is looked up on the first call on each device (with that
- * device current), so make that first call before any stream capture.  All
- * calls share the array: calls that overlap on the GPU (other streams, other
- * threads) race and must be ordered by the caller.  Nothing in it has to start
- * at zero: each call's first pass writes every word its second pass reads.
+ * Its device address is looked up on every call, with the caller's device
+ * current; the first call on a device may load the library's device code
+ * there, so make that first call before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU (other streams, other threads) race
+ * and must be ordered by the caller.  Nothing in it has to start at zero: each
+ * call's first pass writes every word its second pass reads.
  * Uses the current device.  n must be a multiple of 16 in [16,
  * KVC_NOALLOC_MAX_ELEMS], else KVC_EINVAL. */
 #define KVC_NOALLOC_SCRATCH_WORDS 256

@@ -33,8 +33,11 @@ class KvcCache(ctypes.Structure):
         ("k", _vp), ("v", _vp), ("k_scale", _vp), ("v_scale", _vp),
         ("k_gscale", _vp), ("v_gscale", _vp), ("dev_ws", _vp),
         ("attn_ws", _vp), ("attn_ws_bytes", ctypes.c_uint64),
-        ("scrub_on_evict", _i32), ("init_magic", _i32),
+        ("stage", _vp), ("stage_bytes", ctypes.c_uint64),
+        ("scrub_on_evict", _i32), ("rope_offset_frames", _i32),
+        ("init_magic", _i32), ("shot", _i32),
         ("chunk_of_region", _i64 * (1 + KVC_MAX_WINDOW)),
+        ("frame0_of_region", _i64 * (1 + KVC_MAX_WINDOW)),
         ("last_chunk", _i64),
     ]
 
@@ -45,10 +48,13 @@ SIGNATURES = {
     "kvc_cache_bytes": (ctypes.c_size_t, [ctypes.POINTER(KvcCache), _i32]),
     "kvc_init": (_i32, [ctypes.POINTER(KvcCache)]),
     "kvc_append": (_i32, [ctypes.POINTER(KvcCache), _vp, _vp, _i64, _vp]),
+    "kvc_append_shot": (_i32, [ctypes.POINTER(KvcCache), _vp, _vp, _i64, _vp]),
     "kvc_evict": (_i32, [ctypes.POINTER(KvcCache), _i64, _vp]),
     "sinkwin_attn": (_i32, [ctypes.POINTER(KvcCache), _vp, _vp, _i32, ctypes.c_float, _vp]),
     "kvc_recache": (_i32, [ctypes.POINTER(KvcCache), _vp, _vp, _vp, ctypes.c_float,
                            ctypes.POINTER(_i64), _i32, _i32, _i32, ctypes.c_float, _vp]),
+    "kvc_project_append": (_i32, [ctypes.POINTER(KvcCache), _vp, _vp, _vp, _vp, ctypes.c_float,
+                                  _i64, _i32, _i32, _i32, ctypes.c_float, _vp, _vp]),
     "kvc_quant_fp4": (_i32, [_vp, _i64, _vp, _vp, _vp, _vp, _vp]),
     "kvc_quant_fp4_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _vp]),
     "kvc_last_device_error": (_i32, [ctypes.POINTER(KvcCache), _vp]),

@@ -47,7 +47,10 @@ class KVCache:
 
     def __init__(self, heads: int, head_dim: int, tokens_per_frame: int, chunk_frames: int,
                  window_chunks: int, dtype: str = "bf16", device="cuda", scrub_on_evict=False,
-                 attn_workspace: bool = True):
+                 attn_workspace: bool = True, stage: bool | int = False, rope_offset_frames: int = 0):
+        """stage: False (none), True (the largest any call needs, kvc_cache_bytes(c, 8)) or a
+        size in bytes -- the staging buffer kvc_recache on an FP4 cache and
+        kvc_project_append use.  rope_offset_frames: the multi-shot RoPE offset."""
         self.c = KvcCache()
         c = self.c
         c.heads, c.head_dim = heads, head_dim
@@ -55,6 +58,7 @@ class KVCache:
         c.window_chunks = window_chunks
         c.dtype = {"bf16": KVC_BF16, "fp4": KVC_FP4}[dtype]
         c.scrub_on_evict = 1 if scrub_on_evict else 0
+        c.rope_offset_frames = int(rope_offset_frames)
         self.dtype = dtype
         self.device = _cuda_device(device)
         self.H, self.D = heads, head_dim
@@ -62,7 +66,7 @@ class KVCache:
         self.W = window_chunks
         self.S = (1 + window_chunks) * self.Tc
         L = lib()
-        nbytes = [L.kvc_cache_bytes(ctypes.byref(c), i) for i in range(8)]
+        nbytes = [L.kvc_cache_bytes(ctypes.byref(c), i) for i in range(9)]
         if nbytes[0] == 0:
             raise ValueError("invalid cache geometry")
         if dtype == "bf16":
@@ -83,6 +87,10 @@ class KVCache:
                         if attn_workspace and nbytes[7] > 0 else None)
         c.attn_ws = 0 if self.attn_ws is None else self.attn_ws.data_ptr()
         c.attn_ws_bytes = 0 if self.attn_ws is None else nbytes[7]
+        sb = nbytes[8] if stage is True else int(stage or 0)
+        self.stage = torch.empty(sb, dtype=torch.uint8, device=self.device) if sb > 0 else None
+        c.stage = 0 if self.stage is None else self.stage.data_ptr()
+        c.stage_bytes = sb
         for name, t, nb in (("k", self.k, nbytes[0]), ("v", self.v, nbytes[1]),
                             ("k_scale", self.k_scale, nbytes[2]), ("v_scale", self.v_scale, nbytes[3]),
                             ("k_gscale", self.k_gscale, nbytes[4]), ("v_gscale", self.v_gscale, nbytes[5]),
@@ -98,6 +106,14 @@ class KVCache:
     def chunk_of_region(self) -> list[int]:
         return [int(self.c.chunk_of_region[i]) for i in range(1 + self.W)]
 
+    @property
+    def frame0_of_region(self) -> list[int]:
+        return [int(self.c.frame0_of_region[i]) for i in range(1 + self.W)]
+
+    @property
+    def shot(self) -> int:
+        return int(self.c.shot)
+
     # -- calls ---------------------------------------------------------------
     # Every call runs with the cache's device current and on that device's stream:
     # the library launches on the current device, with the pointers it is given.
@@ -108,6 +124,38 @@ class KVCache:
         with torch.cuda.device(self.device):
             check(lib().kvc_append(ctypes.byref(self.c), _ptr(k), _ptr(v), int(chunk_idx),
                                    _stream(self.device, stream)), "kvc_append")
+
+    def append_shot(self, k: torch.Tensor, v: torch.Tensor, chunk_idx: int, stream=None) -> None:
+        """Append chunk_idx as the first chunk of a new shot (it becomes the sink)."""
+        shp = (self.Tc, self.H, self.D)
+        _require(k, torch.bfloat16, shp, "k", self.device)
+        _require(v, torch.bfloat16, shp, "v", self.device)
+        with torch.cuda.device(self.device):
+            check(lib().kvc_append_shot(ctypes.byref(self.c), _ptr(k), _ptr(v), int(chunk_idx),
+                                        _stream(self.device, stream)), "kvc_append_shot")
+
+    def project_append(self, hidden: torch.Tensor, w_qkv: torch.Tensor, gamma_q, gamma_k,
+                       chunk_idx: int, grid_h: int, grid_w: int, eps: float = 1e-6,
+                       theta: float = 10000.0, new_shot: bool = False, q_out=None,
+                       stream=None) -> torch.Tensor:
+        """[Q|K|V] = hidden @ w_qkv with Q/K RMSNorm + 3D RoPE; K, V appended as
+        chunk_idx; returns Q [Tc][H][D] bf16."""
+        HD = self.H * self.D
+        _require(hidden, torch.bfloat16, (self.Tc, HD), "hidden", self.device)
+        _require(w_qkv, torch.bfloat16, (HD, 3 * HD), "w_qkv", self.device)
+        for name, g in (("gamma_q", gamma_q), ("gamma_k", gamma_k)):
+            if g is not None:
+                _require(g, torch.float32, (HD,), name, self.device)
+        if q_out is None:
+            q_out = torch.empty((self.Tc, self.H, self.D), dtype=torch.bfloat16, device=self.device)
+        _require(q_out, torch.bfloat16, (self.Tc, self.H, self.D), "q_out", self.device)
+        with torch.cuda.device(self.device):
+            check(lib().kvc_project_append(ctypes.byref(self.c), _ptr(hidden), _ptr(w_qkv),
+                                           _ptr(gamma_q), _ptr(gamma_k), float(eps), int(chunk_idx),
+                                           1 if new_shot else 0, int(grid_h), int(grid_w),
+                                           float(theta), _ptr(q_out), _stream(self.device, stream)),
+                  "kvc_project_append")
+        return q_out
 
     def evict(self, chunk_idx: int, stream=None) -> None:
         with torch.cuda.device(self.device):

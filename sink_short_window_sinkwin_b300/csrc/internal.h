@@ -71,21 +71,37 @@ size_t attn_workspace_bytes(int D, int ctas);
 // SMs of the current device (0 when there is none)
 int attn_sm_count();
 
-// ---- recache (kernels_recache.cu) ----
+// ---- projection GEMMs + norm/RoPE (kernels_recache.cu) ----
 struct RecacheLaunch {
   const void* hidden;  // bf16 [n*Tc][H*D]
   const void* w_kv;    // bf16 [H*D][2*H*D]
   const float* gamma;  // fp32 [H*D] or null
   float eps, theta;
-  int32_t rows, H, D, Tc, tpf, chunk_frames, grid_w;
+  int32_t rows, H, D, Tc, tpf, grid_w;
   int32_t n;
-  int64_t chunk_id[kMaxSeg];
-  int32_t region[kMaxSeg];
-  void* k;  // bf16 cache [S][H][D]
+  int64_t frame0[kMaxSeg];  // RoPE frame position of each chunk's first frame
+  int32_t region[kMaxSeg];  // destination region of each chunk
+  void* k;  // bf16 [regions * Tc][H][D]: the cache, or a staging buffer
   void* v;
   int32_t* dev_err;
 };
 cudaError_t launch_recache(const RecacheLaunch& r, cudaStream_t st);
+// Q, K, V of one chunk: [Q|K|V] = hidden @ w_qkv, Q and K normed + rotated.
+struct ProjectLaunch {
+  const void* hidden;  // bf16 [Tc][H*D]
+  const void* w_qkv;   // bf16 [H*D][3*H*D]
+  const float* gamma_q;
+  const float* gamma_k;
+  float eps, theta;
+  int32_t Tc, H, D, tpf, grid_w;
+  int64_t frame0;
+  float* stage_f32;  // [Tc][2*H*D] fp32 scratch
+  void* q_out;       // bf16 [Tc][H*D]
+  void* k_dst;       // bf16 [Tc][H*D]
+  void* v_dst;       // bf16 [Tc][H*D]
+  int32_t* dev_err;
+};
+cudaError_t launch_project_chunk(const ProjectLaunch& r, cudaStream_t st);
 // H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} and D even, D/2 <= 128
 bool recache_supported(int H, int D);
 

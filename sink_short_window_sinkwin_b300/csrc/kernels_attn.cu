@@ -9,13 +9,15 @@
 // Work: an "item" is one head x two 128-row query tiles ("slots") that share
 // every K/V tile; a "step" is one item x one 128-key K/V tile.  The kernel is
 // persistent: G CTAs (at most one per SM) each take an equal contiguous share
-// of all items' steps, so the last wave is as full as the first.  An item cut
-// by a share boundary is computed in two pieces by neighbouring CTAs: CTA g+1
-// (whose share starts inside the item) writes its piece's unnormalised O and
-// (max, sum) rows to a workspace slot and raises a flag; CTA g (whose share
-// ends inside the item, and which reaches that piece last) waits for the flag
-// -- a bounded wait, in a cooperative launch -- and merges the two pieces.
-// Without a workspace the shares are whole items.
+// of all items' steps, so the last wave is as full as the first.  With fewer
+// items than SMs (a short query chunk), G still covers every SM and an item is
+// spread over several shares (split-KV).  An item cut by share boundaries is
+// computed in pieces by neighbouring CTAs: every CTA g' > g whose share starts
+// inside the item writes its piece's unnormalised O and (max, sum) rows to its
+// workspace slot and raises a flag; CTA g (whose share ends inside the item, and
+// which reaches that piece last) waits for those flags -- bounded waits, in a
+// cooperative launch -- and merges the pieces.  Without a workspace the shares
+// are whole items.
 //
 // Warp roles (320 threads; 448 with an FP4 cache):
 //   warps 0-3  softmax of slot 0 (thread i owns query row i: TMEM lane i)
@@ -46,6 +48,7 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDequantWarp0 = 10;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMinShareSteps = 8;          // K/V tiles per share at least (split-KV)
 
 struct AttnParams {
   int32_t tq, H, D, S, nt;  // nt: K/V tiles of one item (over all segments)
@@ -117,13 +120,21 @@ struct KvCursor {
 // Softmax does not see key order, so a piece may visit its item's K/V tiles in
 // any order.  Tiles are visited rotated so that at local step tau of every
 // share the tile is about tau mod nt: CTAs working on the same head then read
-// the same tile at about the same time and share it through L2.  Both pieces
-// of a split item take the rotation of the piece that ends it (its share
-// starts with it), so together they still visit every tile once.
+// the same tile at about the same time and share it through L2.  All pieces of
+// a split item take the rotation of the piece that ends it (its share starts
+// with it), so together they still visit every tile once.
 struct Piece {
   int u, t0, t1;
   int rot;  // physical tile of logical tile t is (t + rot) mod nt
 };
+// First step of share g, and the share holding step s (shares are never empty:
+// G <= NS).
+__device__ __forceinline__ int64_t share_begin(const AttnParams& p, int g) {
+  return p.split ? (int64_t)g * p.NS / p.G : ((int64_t)g * p.NI / p.G) * p.nt;
+}
+__device__ __forceinline__ int share_of_step(const AttnParams& p, int64_t s) {
+  return (int)(((s + 1) * p.G + p.NS - 1) / p.NS) - 1;
+}
 struct Share {
   int64_t b, s, e;
   __device__ __forceinline__ bool next(const AttnParams& p, Piece& pc) {
@@ -131,9 +142,15 @@ struct Share {
     pc.u = (int)(s / p.nt);
     pc.t0 = (int)(s - (int64_t)pc.u * p.nt);
     pc.t1 = (int)min((int64_t)p.nt, pc.t0 + (e - s));
-    if (pc.t0 > 0) pc.rot = (p.nt - pc.t0) % p.nt;        // ends an item started elsewhere
-    else if (pc.t1 < p.nt) pc.rot = (p.nt - pc.t1) % p.nt;  // starts an item finished elsewhere
-    else pc.rot = (int)((s - b) % p.nt);                    // a whole item
+    const int64_t ib = (int64_t)pc.u * p.nt;  // the item's first step
+    if (ib >= b && ib + p.nt <= e) {
+      pc.rot = (int)((s - b) % p.nt);  // a whole item
+    } else {
+      // the item's last piece starts the share holding its last step
+      const int64_t tb = share_begin(p, share_of_step(p, ib + p.nt - 1));
+      const int t0_tail = (int)(tb > ib ? tb - ib : 0);
+      pc.rot = (p.nt - t0_tail) % p.nt;
+    }
     s += pc.t1 - pc.t0;
     return true;
   }
@@ -143,12 +160,8 @@ struct Share {
   }
 };
 __device__ __forceinline__ Share share_of(const AttnParams& p, int g) {
-  if (p.split) {
-    const int64_t b = (int64_t)g * p.NS / p.G;
-    return Share{b, b, (int64_t)(g + 1) * p.NS / p.G};
-  }
-  const int64_t a = (int64_t)g * p.NI / p.G, z = (int64_t)(g + 1) * p.NI / p.G;
-  return Share{a * p.nt, a * p.nt, z * p.nt};
+  const int64_t b = share_begin(p, g);
+  return Share{b, b, g + 1 < p.G ? share_begin(p, g + 1) : (p.split ? p.NS : (int64_t)p.NI * p.nt)};
 }
 
 // ---------------------------------------------------------------------------
@@ -747,41 +760,42 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       const int prow = slot * BM + row;  // row within the item's 256
       const int grow = m0 + prow;
       const bool head = pc.t0 == 0, tail = pc.t1 == p.nt;
-      const float* wsb = nullptr;  // partner piece to merge (head && !tail)
-      float mo = 0.0f, lo = 0.0f;
+      // head && !tail: the item's later pieces are in the workspace slots of
+      // shares g+1 .. gt; wait for each, then merge all of them
+      int gt = g;
+      float mm = m_ref, inv_l = 0.0f;
       if (head && !tail) {
-        // the share's last piece, starting this item: merge with CTA g+1's
-        const unsigned long long* f = p.ws_flag + g + 1;
-        const uint64_t t0 = globaltimer_ns();
+        gt = share_of_step(p, (int64_t)(pc.u + 1) * p.nt - 1);
         bool got = true;
-        while (ld_acquire_gpu_u64(f) != p.epoch) {
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            sm.abort_flag = 1;
-            if (p.dev_err) atomicCAS(p.dev_err, DEVERR_NONE, DEVERR_TIMEOUT);
-            got = false;
-            break;
+        for (int q = g + 1; q <= gt && got; ++q) {
+          const unsigned long long* f = p.ws_flag + q;
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu_u64(f) != p.epoch) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              sm.abort_flag = 1;
+              if (p.dev_err) atomicCAS(p.dev_err, DEVERR_NONE, DEVERR_TIMEOUT);
+              got = false;
+              break;
+            }
           }
         }
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        wsb = p.ws_o + ((size_t)(g + 1) * 2 * BM + prow) * D;
-        const float2 ml = p.ws_ml[(size_t)(g + 1) * 2 * BM + prow];
-        mo = ml.x;
-        lo = ml.y;
-      }
-      float fa = 1.0f, fb = 0.0f, inv_l = 0.0f;
-      if (head && !tail) {
-        const float mm = fmaxf(m_ref, mo);
-        fa = ex2_approx(m_ref - mm);
-        fb = ex2_approx(mo - mm);
-        inv_l = 1.0f / (l * fa + lo * fb);
+        for (int q = g + 1; q <= gt; ++q) mm = fmaxf(mm, p.ws_ml[(size_t)q * 2 * BM + prow].x);
+        float lt = l * ex2_approx(m_ref - mm);
+        for (int q = g + 1; q <= gt; ++q) {
+          const float2 ml = p.ws_ml[(size_t)q * 2 * BM + prow];
+          lt += ml.y * ex2_approx(ml.x - mm);
+        }
+        inv_l = 1.0f / lt;
       } else if (head) {
         inv_l = 1.0f / l;
       }
+      const float fa = ex2_approx(m_ref - mm);  // 1 unless merging
       if constexpr (kFp4) inv_l *= v_shift;
-      float* wsw = nullptr;  // this piece handed to CTA g-1 (!head)
+      float* wsw = nullptr;  // this piece handed to the CTA that started the item (!head)
       if (!head) {
         wsw = p.ws_o + ((size_t)g * 2 * BM + prow) * D;
         p.ws_ml[(size_t)g * 2 * BM + prow] = make_float2(m_ref, l);
@@ -801,20 +815,23 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           continue;
         }
         float x[32];
-        if (!tail) {
-          const float4* r4 = reinterpret_cast<const float4*>(wsb + j * 32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]) * fa;
+#pragma unroll 1
+        for (int q = g + 1; q <= gt; ++q) {
+          const float fb = ex2_approx(p.ws_ml[(size_t)q * 2 * BM + prow].x - mm);
+          const float4* r4 = reinterpret_cast<const float4*>(p.ws_o + ((size_t)q * 2 * BM + prow) * D + j * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 b = r4[e];
-            x[4 * e + 0] = (__uint_as_float(o[4 * e + 0]) * fa + b.x * fb) * inv_l;
-            x[4 * e + 1] = (__uint_as_float(o[4 * e + 1]) * fa + b.y * fb) * inv_l;
-            x[4 * e + 2] = (__uint_as_float(o[4 * e + 2]) * fa + b.z * fb) * inv_l;
-            x[4 * e + 3] = (__uint_as_float(o[4 * e + 3]) * fa + b.w * fb) * inv_l;
+            x[4 * e + 0] = fmaf(b.x, fb, x[4 * e + 0]);
+            x[4 * e + 1] = fmaf(b.y, fb, x[4 * e + 1]);
+            x[4 * e + 2] = fmaf(b.z, fb, x[4 * e + 2]);
+            x[4 * e + 3] = fmaf(b.w, fb, x[4 * e + 3]);
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]) * inv_l;
         }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] *= inv_l;
         if (grow < p.tq) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
@@ -905,21 +922,28 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   p.vg = a.v_gscale;
   p.Tc = a.chunk_tokens;
   for (int i = 0; i < a.nseg; ++i) p.seg_region[i] = p.Tc > 0 ? a.seg[i].row0 / p.Tc : 0;
-  // schedule: at most one CTA per SM and per item, so every item spans at
-  // most two neighbouring shares
+  // schedule: at most one CTA per SM.  With the workspace, shares are
+  // step-balanced and an item may spread over several shares (at least
+  // kMinShareSteps K/V tiles each); without it every CTA takes whole items.
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   p.n_pairs = (a.tq + 2 * BM - 1) / (2 * BM);
   p.NI = p.n_pairs * a.H;
   p.NS = (int64_t)p.NI * nt;
-  p.G = p.NI < nsm ? p.NI : nsm;
-  const size_t need = attn_workspace_bytes(a.D, p.G);
-  p.split = (a.ws != nullptr && a.ws_bytes >= need && p.G > 1 && p.NI % p.G != 0) ? 1 : 0;
+  const size_t need = attn_workspace_bytes(a.D, nsm);
+  const bool have_ws = a.ws != nullptr && a.ws_bytes >= need;
+  int64_t G = have_ws ? p.NS / kMinShareSteps : p.NI;
+  if (G > nsm) G = nsm;
+  if (G > p.NS) G = p.NS;
+  if (G < 1) G = 1;
+  p.G = (int32_t)G;
+  p.split = (have_ws && p.G > 1 && (p.G > p.NI || p.NI % p.G != 0)) ? 1 : 0;
+  if (!p.split && p.G > p.NI) p.G = p.NI;
   if (p.split) {
     uint8_t* w = static_cast<uint8_t*>(a.ws);
     p.ws_o = reinterpret_cast<float*>(w);
-    p.ws_ml = reinterpret_cast<float2*>(w + (size_t)p.G * 2 * BM * a.D * 4);
-    p.ws_flag = reinterpret_cast<unsigned long long*>(w + (size_t)p.G * 2 * BM * (a.D * 4 + 8));
+    p.ws_ml = reinterpret_cast<float2*>(w + (size_t)nsm * 2 * BM * a.D * 4);
+    p.ws_flag = reinterpret_cast<unsigned long long*>(w + (size_t)nsm * 2 * BM * (a.D * 4 + 8));
     static std::atomic<unsigned long long> epochs{0};
     p.epoch = epochs.fetch_add(1) + 1;
   }

@@ -116,7 +116,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool ready(const kvc_cache* c) { return c && c->init_magic == KVC_INIT_MAGIC && geometry_ok(c); }
 
-int32_t region_of(int64_t chunk, int32_t W) { return chunk == 0 ? 0 : 1 + (int32_t)((chunk - 1) % W); }
+// Region of a chunk: 0 for the sink (chunk 0, or a shot's first chunk once it
+// is the sink), else its ring slot.
+int32_t region_of(const kvc_cache* c, int64_t chunk) {
+  if (chunk == 0 || chunk == c->chunk_of_region[0]) return 0;
+  return 1 + (int32_t)((chunk - 1) % c->window_chunks);
+}
+
+// RoPE frame position of a chunk's first frame, `shot` boundaries in.
+int64_t frame0_of(const kvc_cache* c, int64_t chunk, int32_t shot) {
+  return chunk * c->chunk_frames + (int64_t)shot * c->rope_offset_frames;
+}
 
 int64_t oldest_window_chunk(const kvc_cache* c) {
   int64_t m = -1;
@@ -130,8 +140,8 @@ int64_t oldest_window_chunk(const kvc_cache* c) {
 // present chunks in logical order: sink first, then window chunks ascending
 int present_chunks(const kvc_cache* c, int64_t* out) {
   int n = 0;
-  if (c->chunk_of_region[0] == 0) out[n++] = 0;
-  int64_t last = 0;
+  if (c->chunk_of_region[0] >= 0) out[n++] = c->chunk_of_region[0];
+  int64_t last = -1;
   while (true) {
     int64_t best = -1;
     for (int r = 1; r <= c->window_chunks; ++r) {
@@ -161,6 +171,53 @@ size_t row_bytes(const kvc_cache* c, int which) {
   }
 }
 
+// bytes of one chunk of fp32 rows of width H*D
+size_t chunk_f32_bytes(const kvc_cache* c) {
+  return (size_t)chunk_tokens(c) * c->heads * c->head_dim * 4;
+}
+
+bool stage_ok(const kvc_cache* c, size_t need) {
+  return c->stage && aligned16(c->stage) && c->stage_bytes >= need;
+}
+
+// Copy (bf16) or FP4-encode one chunk's K and V into region r.
+cudaError_t store_chunk(kvc_cache* c, const void* k, const void* v, int32_t r, cudaStream_t st) {
+  const int64_t Tc = chunk_tokens(c);
+  const int64_t n = Tc * c->heads * (int64_t)c->head_dim;  // elements per tensor
+  if (c->dtype == KVC_BF16) {
+    const size_t off = (size_t)r * Tc * row_bytes(c, 0);
+    return launch_copy2(static_cast<uint8_t*>(c->k) + off, k, static_cast<uint8_t*>(c->v) + off, v,
+                        (size_t)n * 2, st);
+  }
+  const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
+  const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
+  QuantJob jobs[2] = {{k, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
+                      {v, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
+  return launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
+}
+
+// State check of an append of chunk_idx (as a new shot's sink when `shot`):
+// the region it goes to, or -1 when the call is not valid now.
+int32_t append_region(const kvc_cache* c, int64_t chunk_idx, bool shot) {
+  if (shot) {
+    if (chunk_idx == c->last_chunk + 1) return (chunk_idx > 0 || c->chunk_of_region[0] == -1) ? 0 : -1;
+    return (chunk_idx == c->last_chunk && c->chunk_of_region[0] == chunk_idx) ? 0 : -1;
+  }
+  const int32_t r = region_of(c, chunk_idx);
+  const int64_t occ = c->chunk_of_region[r];
+  if (chunk_idx == c->last_chunk + 1) return occ == -1 ? r : -1;  // next chunk: needs a free slot
+  return (chunk_idx == c->last_chunk && occ == chunk_idx) ? r : -1;  // overwrite while cached
+}
+
+// Commit an append's state (after its launches succeeded).
+void commit_append(kvc_cache* c, int64_t chunk_idx, int32_t r, bool shot) {
+  const bool fresh = c->chunk_of_region[r] != chunk_idx;
+  if (shot && fresh && chunk_idx > 0) c->shot += 1;
+  if (fresh) c->frame0_of_region[r] = frame0_of(c, chunk_idx, c->shot);
+  c->chunk_of_region[r] = chunk_idx;
+  c->last_chunk = chunk_idx;
+}
+
 }  // namespace
 
 extern "C" {
@@ -185,6 +242,10 @@ size_t kvc_cache_bytes(const kvc_cache* c, int32_t which) {
       const int nsm = attn_sm_count();
       return nsm > 0 ? attn_workspace_bytes(c->head_dim, nsm) : 0;
     }
+    case 8: {
+      const size_t m = 1 + (size_t)c->window_chunks;
+      return chunk_f32_bytes(c) * (m > 3 ? m : 3);
+    }
     default:
       return 0;
   }
@@ -195,58 +256,50 @@ int32_t kvc_init(kvc_cache* c) {
   if (!c->k || !c->v || !c->dev_ws || !aligned16(c->k) || !aligned16(c->v) || !aligned16(c->dev_ws))
     return KVC_EINVAL;
   if (c->attn_ws && !aligned16(c->attn_ws)) return KVC_EINVAL;
+  if (c->stage && !aligned16(c->stage)) return KVC_EINVAL;
   if (c->dtype == KVC_FP4) {
     if (!c->k_scale || !c->v_scale || !c->k_gscale || !c->v_gscale) return KVC_EINVAL;
     if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVC_EINVAL;
     if ((reinterpret_cast<uintptr_t>(c->k_gscale) & 3u) || (reinterpret_cast<uintptr_t>(c->v_gscale) & 3u))
       return KVC_EINVAL;
   }
-  for (int r = 0; r < 1 + KVC_MAX_WINDOW; ++r) c->chunk_of_region[r] = -1;
+  for (int r = 0; r < 1 + KVC_MAX_WINDOW; ++r) {
+    c->chunk_of_region[r] = -1;
+    c->frame0_of_region[r] = -1;
+  }
   c->last_chunk = -1;
+  c->shot = 0;
   c->init_magic = KVC_INIT_MAGIC;
+  return KVC_OK;
+}
+
+static int32_t append_impl(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
+                           kvc_stream_t stream, bool shot) {
+  if (!ready(c) || !k_chunk || !v_chunk || !aligned16(k_chunk) || !aligned16(v_chunk) || chunk_idx < 0)
+    return KVC_EINVAL;
+  const int32_t r = append_region(c, chunk_idx, shot);
+  if (r < 0) return KVC_ESTATE;
+  if (store_chunk(c, k_chunk, v_chunk, r, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ECUDA;
+  commit_append(c, chunk_idx, r, shot);
   return KVC_OK;
 }
 
 int32_t kvc_append(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
                    kvc_stream_t stream) {
-  if (!ready(c) || !k_chunk || !v_chunk || !aligned16(k_chunk) || !aligned16(v_chunk) || chunk_idx < 0)
-    return KVC_EINVAL;
-  // state: the next chunk, or the last one again while it is still cached
-  const int32_t r = region_of(chunk_idx, c->window_chunks);
-  const int64_t occ = c->chunk_of_region[r];
-  if (chunk_idx == c->last_chunk + 1) {
-    if (occ != -1) return KVC_ESTATE;  // the slot still holds an older chunk
-  } else if (!(chunk_idx == c->last_chunk && occ == chunk_idx)) {
-    return KVC_ESTATE;
-  }
-  // launch
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t Tc = chunk_tokens(c);
-  const int64_t n = Tc * c->heads * (int64_t)c->head_dim;  // elements per tensor
-  cudaError_t e;
-  if (c->dtype == KVC_BF16) {
-    const size_t off = (size_t)r * Tc * row_bytes(c, 0);
-    e = launch_copy2(static_cast<uint8_t*>(c->k) + off, k_chunk, static_cast<uint8_t*>(c->v) + off,
-                     v_chunk, (size_t)n * 2, st);
-  } else {
-    const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
-    const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
-    QuantJob jobs[2] = {
-        {k_chunk, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
-        {v_chunk, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
-    e = launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
-  }
-  if (e != cudaSuccess) return KVC_ECUDA;
-  c->chunk_of_region[r] = chunk_idx;
-  c->last_chunk = chunk_idx;
-  return KVC_OK;
+  return append_impl(c, k_chunk, v_chunk, chunk_idx, stream, false);
+}
+
+int32_t kvc_append_shot(kvc_cache* c, const void* k_chunk, const void* v_chunk, int64_t chunk_idx,
+                        kvc_stream_t stream) {
+  return append_impl(c, k_chunk, v_chunk, chunk_idx, stream, true);
 }
 
 int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream) {
   if (!ready(c) || chunk_idx < 0) return KVC_EINVAL;
   if (chunk_idx == 0) return KVC_ESTATE;
   if (oldest_window_chunk(c) != chunk_idx) return KVC_ESTATE;
-  const int32_t r = region_of(chunk_idx, c->window_chunks);
+  const int32_t r = 1 + (int32_t)((chunk_idx - 1) % c->window_chunks);
   if (c->chunk_of_region[r] != chunk_idx) return KVC_ESTATE;
   if (c->scrub_on_evict) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -271,6 +324,7 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream) {
     if (e != cudaSuccess) return KVC_ECUDA;
   }
   c->chunk_of_region[r] = -1;
+  c->frame0_of_region[r] = -1;
   return KVC_OK;
 }
 
@@ -282,7 +336,7 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, f
       softmax_scale < 0.0f)
     return KVC_EINVAL;
   if (c->head_dim != 64 && c->head_dim != 128) return KVC_EUNSUPPORTED;
-  if (c->chunk_of_region[0] != 0) return KVC_ESTATE;
+  if (c->chunk_of_region[0] < 0) return KVC_ESTATE;
   AttnLaunch a{};
   a.q = q;
   a.out = out;
@@ -327,13 +381,15 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
   if (grid_h < 1 || grid_w < 1 || (int64_t)grid_h * grid_w != c->tokens_per_frame) return KVC_EINVAL;
   if (!(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta > 0.0f) || !std::isfinite(rope_theta))
     return KVC_EINVAL;
-  if (c->dtype != KVC_BF16) return KVC_EUNSUPPORTED;
   if (!recache_supported(c->heads, c->head_dim)) return KVC_EUNSUPPORTED;
+  const bool fp4 = c->dtype == KVC_FP4;
+  if (fp4 && !stage_ok(c, (size_t)n * chunk_f32_bytes(c))) return KVC_EINVAL;
   int64_t present[1 + KVC_MAX_WINDOW];
   const int np = present_chunks(c, present);
   if (np != n) return KVC_ESTATE;
   for (int i = 0; i < n; ++i)
     if (chunk_ids[i] != present[i]) return KVC_ESTATE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   RecacheLaunch rl{};
   rl.hidden = hidden;
   rl.w_kv = w_kv;
@@ -345,17 +401,80 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
   rl.H = c->heads;
   rl.D = c->head_dim;
   rl.tpf = c->tokens_per_frame;
-  rl.chunk_frames = c->chunk_frames;
   rl.grid_w = grid_w;
   rl.n = n;
   for (int i = 0; i < n; ++i) {
-    rl.chunk_id[i] = chunk_ids[i];
-    rl.region[i] = region_of(chunk_ids[i], c->window_chunks);
+    const int32_t r = region_of(c, chunk_ids[i]);
+    rl.frame0[i] = c->frame0_of_region[r];
+    // FP4: bf16 K and V of chunk i go to rows [i Tc, (i+1) Tc) of the staging buffer
+    rl.region[i] = fp4 ? i : r;
   }
-  rl.k = c->k;
-  rl.v = c->v;
+  const size_t hd2 = (size_t)rl.Tc * c->heads * c->head_dim * 2;  // bf16 bytes of one chunk
+  rl.k = fp4 ? c->stage : c->k;
+  rl.v = fp4 ? static_cast<uint8_t*>(c->stage) + (size_t)n * hd2 : c->v;
   rl.dev_err = c->dev_ws;
-  return cuda_status(launch_recache(rl, reinterpret_cast<cudaStream_t>(stream)));
+  cudaError_t e = launch_recache(rl, st);
+  if (e != cudaSuccess || !fp4) return cuda_status(e);
+  for (int i = 0; i < n; ++i) {
+    const uint8_t* ks = static_cast<const uint8_t*>(rl.k) + (size_t)i * hd2;
+    const uint8_t* vs = static_cast<const uint8_t*>(rl.v) + (size_t)i * hd2;
+    e = store_chunk(c, ks, vs, region_of(c, chunk_ids[i]), st);
+    if (e != cudaSuccess) return KVC_ECUDA;
+  }
+  return KVC_OK;
+}
+
+int32_t kvc_project_append(kvc_cache* c, const void* hidden, const void* w_qkv,
+                           const float* gamma_q, const float* gamma_k, float eps,
+                           int64_t chunk_idx, int32_t new_shot, int32_t grid_h, int32_t grid_w,
+                           float rope_theta, void* q_out, kvc_stream_t stream) {
+  if (!ready(c) || !hidden || !w_qkv || !q_out || chunk_idx < 0) return KVC_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_qkv) || !aligned16(q_out) ||
+      (gamma_q && !aligned16(gamma_q)) || (gamma_k && !aligned16(gamma_k)))
+    return KVC_EINVAL;
+  if (grid_h < 1 || grid_w < 1 || (int64_t)grid_h * grid_w != c->tokens_per_frame) return KVC_EINVAL;
+  if (!(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta > 0.0f) || !std::isfinite(rope_theta))
+    return KVC_EINVAL;
+  if (!recache_supported(c->heads, c->head_dim)) return KVC_EUNSUPPORTED;
+  const bool fp4 = c->dtype == KVC_FP4;
+  const size_t f32b = chunk_f32_bytes(c);  // one chunk of fp32 rows
+  if (!stage_ok(c, 2 * f32b + (fp4 ? f32b : 0))) return KVC_EINVAL;
+  const bool shot = new_shot != 0;
+  const int32_t r = append_region(c, chunk_idx, shot);
+  if (r < 0) return KVC_ESTATE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t Tc = chunk_tokens(c);
+  ProjectLaunch pl{};
+  pl.hidden = hidden;
+  pl.w_qkv = w_qkv;
+  pl.gamma_q = gamma_q;
+  pl.gamma_k = gamma_k;
+  pl.eps = eps;
+  pl.theta = rope_theta;
+  pl.Tc = (int32_t)Tc;
+  pl.H = c->heads;
+  pl.D = c->head_dim;
+  pl.tpf = c->tokens_per_frame;
+  pl.grid_w = grid_w;
+  // positions: an overwrite keeps the chunk's; a new shot counts one boundary more
+  const bool fresh = c->chunk_of_region[r] != chunk_idx;
+  pl.frame0 = fresh ? frame0_of(c, chunk_idx, c->shot + ((shot && chunk_idx > 0) ? 1 : 0))
+                    : c->frame0_of_region[r];
+  pl.stage_f32 = static_cast<float*>(c->stage);
+  pl.q_out = q_out;
+  if (fp4) {  // bf16 K and V wait in the staging buffer for the FP4 encode
+    pl.k_dst = static_cast<uint8_t*>(c->stage) + 2 * f32b;
+    pl.v_dst = static_cast<uint8_t*>(c->stage) + 2 * f32b + f32b / 2;
+  } else {
+    const size_t off = (size_t)r * Tc * row_bytes(c, 0);
+    pl.k_dst = static_cast<uint8_t*>(c->k) + off;
+    pl.v_dst = static_cast<uint8_t*>(c->v) + off;
+  }
+  pl.dev_err = c->dev_ws;
+  if (launch_project_chunk(pl, st) != cudaSuccess) return KVC_ECUDA;
+  if (fp4 && store_chunk(c, pl.k_dst, pl.v_dst, r, st) != cudaSuccess) return KVC_ECUDA;
+  commit_append(c, chunk_idx, r, shot);
+  return KVC_OK;
 }
 
 int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales, float* gscale,

@@ -17,5 +17,7 @@ from .inputs import (  # noqa: F401
     chunk_qkv_device,
     device_seed,
     recache_inputs,
+    project_inputs,
+    gains,
     bf16_to_f64,
 )

@@ -17,7 +17,7 @@ import torch
 
 # tensor ids inside a seed tuple
 _TID_Q, _TID_K, _TID_V, _TID_OUTLIER_K, _TID_OUTLIER_V = 0, 1, 2, 3, 4
-_TID_HIDDEN, _TID_WKV = 10, 11
+_TID_HIDDEN, _TID_WKV, _TID_WQKV, _TID_GAIN = 10, 11, 12, 13
 
 
 @dataclass(frozen=True)
@@ -158,3 +158,19 @@ def recache_inputs(sh: Shapes, cfg: int, n_chunks: int, w_std: float = 0.02):
 def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     """Exact float64 image of a bfloat16 (or float32) CPU tensor."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def project_inputs(sh: Shapes, cfg: int, chunk: int, w_std: float = 0.02):
+    """One chunk's hidden states [Tc][H*D] ~ N(0,1) and the Q|K|V weight
+    [H*D][3*H*D] ~ N(0, w_std^2) (the same weight for every chunk of a cfg)."""
+    hid = gaussian_bf16((sh.chunk_tokens, sh.model_dim), 1.0, cfg, 1, chunk, _TID_HIDDEN)
+    w = gaussian_bf16((sh.model_dim, 3 * sh.model_dim), w_std, cfg, 1, 0, _TID_WQKV)
+    return hid, w
+
+
+def gains(sh: Shapes, cfg: int):
+    """RMSNorm gains for Q and K, float32 [H*D] each, uniform in [0.5, 1.5]."""
+    g = seed_rng(cfg, 1, 0, _TID_GAIN)
+    gq = g.uniform(0.5, 1.5, sh.model_dim).astype(np.float32)
+    gk = g.uniform(0.5, 1.5, sh.model_dim).astype(np.float32)
+    return torch.from_numpy(gq), torch.from_numpy(gk)

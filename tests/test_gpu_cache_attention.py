@@ -223,6 +223,61 @@ def test_layer_attention_full_size_full_compare(swl):
     assert cache.last_device_error() == swl.KVC_OK
 
 
+@pytest.mark.parametrize("tq", [1, 100, 128, 129, 256, 300, 700])
+@pytest.mark.parametrize("dtype", ["bf16", "fp4"])
+def test_split_kv_short_query_chunks(swl, tq, dtype):
+    """Short query chunks against the full LongLive-1.3B cache (12 heads,
+    18720 keys): 12-36 items on up to 148 CTAs, so every item is spread over
+    several CTAs' shares (split-KV) and merged by the CTA that started it.
+    Every output against the oracle."""
+    sh = LAYER_1P3B
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, dtype=dtype)
+    kk, vv = [], []
+    for c in range(1 + sh.window_chunks):
+        _, k, v = chunk_qkv(sh, 61, 0, c, "rms1" if dtype == "bf16" else "outliers")
+        cache.append(k.cuda(), v.cuda(), c)
+        if dtype == "bf16":
+            kk.append(bf16_to_f64(k)), vv.append(bf16_to_f64(v))
+        else:
+            from oracle import fp4 as ofp4
+            kk.append(ofp4.dequantize(*ofp4.quantize(k.float().numpy())))
+            vv.append(ofp4.dequantize(*ofp4.quantize(v.float().numpy())))
+    kk, vv = np.concatenate(kk), np.concatenate(vv)
+    q = chunk_qkv(sh, 62, 0, tq, "rms1", q_rows=tq)[0]
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oatt.attention(bf16_to_f64(q), kk, vv, scale)
+    if dtype == "bf16":
+        assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, f"split-KV tq={tq}")
+    else:
+        assert_close(to64(out), want, 5e-2, None, f"fp4 split-KV tq={tq}", plus_output_rounding=True)
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_split_kv_planted_max_and_no_workspace(swl):
+    """tq = 130 on the 12-head cache with keys planted in one late tile: the
+    pieces of an item hold maxima ~12 (log2 units) apart.  The same call
+    without a workspace (whole items, 12 CTAs) gives the same answer."""
+    H, D = 12, 128
+    cache, model, u, rng = _planted_stream(swl, H, D, 1560, 3, 3, "late_tile", 63)
+    cache2 = swl.KVCache(H, D, 1560, 3, 3, attn_workspace=False)
+    for c in range(4):
+        r = cache.chunk_of_region.index(c)
+        sl = slice(r * 4680, (r + 1) * 4680)
+        cache2.append(cache.k[sl].contiguous(), cache.v[sl].contiguous(), c)
+    q = 10 * u + 0.3 * rng.standard_normal((130, H, D))
+    qb = torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16).cuda()
+    scale = 1.0 / math.sqrt(D)
+    out, out2 = cache.attn(qb, scale), cache2.attn(qb, scale)
+    torch.cuda.synchronize()
+    want = oatt.sinkwin_attention(model, to64(qb), scale)
+    assert_close(to64(out), want, ATOL_BF16, RELL2_BF16, "split-KV planted")
+    assert_close(to64(out2), want, ATOL_BF16, RELL2_BF16, "whole items planted")
+    assert cache.last_device_error() == swl.KVC_OK and cache2.last_device_error() == swl.KVC_OK
+
+
 def test_holes_scrub_and_zero_queries(swl):
     """Evict without append leaves a hole (two KV segments); the scrubbed slot
     holds NaN and must never reach the output."""

@@ -8,10 +8,12 @@ import pytest
 import torch
 
 from oracle import attention as oatt
+from oracle import fp4 as ofp4
 from oracle import recache as orc
 from oracle.cache_model import CacheModel
 from synth import LAYER_1P3B, TINY, Shapes, chunk_qkv, recache_inputs, bf16_to_f64
-from tests.gpu_helpers import ATOL_BF16, RELL2_BF16, SAMPLE_ROWS_4680, assert_close, to64
+from tests.gpu_helpers import (ATOL_BF16, ATOL_FP4, RELL2_BF16, SAMPLE_ROWS_4680, assert_close,
+                               to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -174,9 +176,110 @@ def test_recache_rejections(swl):
     with pytest.raises(swl.KvcError) as e:
         cache.recache(hid.cuda(), wkv.cuda(), g_off, [0, 1, 2], sh.grid_h, sh.grid_w)
     assert e.value.status == swl.KVC_EINVAL
+    # an FP4 cache recaches through the staging buffer: without one (or with one
+    # too small for the listed chunks) the call is refused
     f = swl.KVCache(1, 64, 16, 2, 2, dtype="fp4")
     z = torch.zeros((32, 1, 64), dtype=torch.bfloat16, device="cuda")
     f.append(z, z, 0)
     with pytest.raises(swl.KvcError) as e:
         f.recache(hid[:32].cuda(), wkv.cuda(), None, [0], 4, 4)
-    assert e.value.status == swl.KVC_EUNSUPPORTED
+    assert e.value.status == swl.KVC_EINVAL
+    f2 = swl.KVCache(1, 64, 16, 2, 2, dtype="fp4", stage=32 * 64 * 4 - 16)
+    f2.append(z, z, 0)
+    with pytest.raises(swl.KvcError) as e:
+        f2.recache(hid[:32].cuda(), wkv.cuda(), None, [0], 4, 4)
+    assert e.value.status == swl.KVC_EINVAL
+
+
+# ---------------------------------------------------------------------------
+# recache into an FP4 cache
+# ---------------------------------------------------------------------------
+def _fill_fp4(swl, sh: Shapes, upto: int):
+    cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, sh.window_chunks,
+                        dtype="fp4", stage=True)
+    model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+    z = torch.zeros((sh.chunk_tokens, sh.heads, sh.head_dim), dtype=torch.bfloat16, device="cuda")
+    zn = np.zeros((sh.chunk_tokens, sh.heads, sh.head_dim))
+    for c in range(upto + 1):
+        if c > sh.window_chunks:
+            cache.evict(c - sh.window_chunks)
+            model.evict(c - sh.window_chunks)
+        cache.append(z, z, c)
+        model.append(c, zn, zn)
+    return cache, model
+
+
+def _check_fp4_recache(swl, sh, upto, cfg, rows=None, what="", q_rows=None):
+    """Recache an FP4 cache, then check (1) every region's codes, block scales
+    and tensor scale are bit-exactly the oracle's encode of the bf16 K/V the
+    kernels left in the staging buffer (one tensor per region); (2) the decoded
+    cache lies within the FP4 reconstruction bound (one E2M1 step at the block's
+    scale) plus the bf16 tolerance of the oracle's float64 recache; (3) attention
+    over the cache matches the oracle run on the oracle's own quantised recache
+    (its float64 K/V rounded to bf16, then encoded per region)."""
+    cache, model = _fill_fp4(swl, sh, upto)
+    ids = model.present_chunks()
+    hid, wkv, gamma = recache_inputs(sh, cfg, len(ids))
+    cache.recache(hid.cuda(), wkv.cuda(), gamma.cuda(), ids, sh.grid_h, sh.grid_w)
+    torch.cuda.synchronize()
+    k64, v64 = orc.recache(bf16_to_f64(hid), bf16_to_f64(wkv), gamma.double().numpy(), ids,
+                           sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames, sh.grid_w)
+    Tc, n = sh.chunk_tokens, len(ids)
+    hd = sh.model_dim
+    st = cache.stage[: 2 * n * Tc * hd * 2].view(torch.bfloat16).view(2, n * Tc, sh.heads, sh.head_dim)
+    st_k, st_v = st[0].float().cpu().numpy(), st[1].float().cpu().numpy()
+    for i, c in enumerate(ids):
+        r = cache.chunk_of_region.index(c)
+        sl_r = slice(r * Tc, (r + 1) * Tc)
+        sl_i = slice(i * Tc, (i + 1) * Tc)
+        sel = np.arange(Tc) if rows is None else np.asarray(rows)
+        for tname, stage_x, cb, sb, gb, ref in (
+                ("K", st_k, cache.k, cache.k_scale, cache.k_gscale, k64),
+                ("V", st_v, cache.v, cache.v_scale, cache.v_gscale, v64)):
+            codes, scales, g = ofp4.quantize(stage_x[sl_i])
+            assert np.array_equal(cb[sl_r].cpu().numpy(), codes), f"{what} {tname} codes, chunk {c}"
+            assert np.array_equal(sb[sl_r].cpu().numpy(), scales), f"{what} {tname} scales, chunk {c}"
+            assert gb[r].item() == float(g), f"{what} {tname} tensor scale, chunk {c}"
+            xh = ofp4.dequantize(cb[sl_r].cpu().numpy(), sb[sl_r].cpu().numpy(), gb[r].item())
+            unit = np.repeat(ofp4.E4M3_ALL[sb[sl_r].cpu().numpy()], 16, axis=-1) * gb[r].item()
+            err = np.abs(xh - ref[sl_i])[sel] - unit[sel]
+            assert err.max() <= ATOL_BF16, f"{what} {tname} chunk {c}: beyond the FP4 bound by {err.max():.3e}"
+    # attention over the recached FP4 cache vs the oracle run on its own
+    # quantised recache: float64 K/V rounded to bf16, encoded per region
+    kk = np.concatenate([ofp4.dequantize(*ofp4.quantize(_bf16_round(k64[i * Tc:(i + 1) * Tc])))
+                         for i in range(n)])
+    vv = np.concatenate([ofp4.dequantize(*ofp4.quantize(_bf16_round(v64[i * Tc:(i + 1) * Tc])))
+                         for i in range(n)])
+    q = chunk_qkv(sh, cfg, 0, 99, "rms1", q_rows=q_rows)[0]
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    out = cache.attn(q.cuda(), scale)
+    torch.cuda.synchronize()
+    qr = SAMPLE_ROWS_4680 if q.shape[0] == 4680 else list(range(q.shape[0]))
+    want = oatt.attention_rows(bf16_to_f64(q), kk, vv, scale, qr)
+    print(assert_close(to64(out)[qr], want, ATOL_FP4, None, f"{what} attention after FP4 recache",
+                       plus_output_rounding=True))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
+def _bf16_round(x: np.ndarray) -> np.ndarray:
+    """float64 -> bf16 (round to nearest even, through float32) -> float32 values."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def test_recache_fp4_tiny(swl):
+    _check_fp4_recache(swl, TINY, 4, 31, what="tiny")
+
+
+def test_recache_fp4_noncontiguous_positions(swl):
+    """H*D = 512 (two GEMM column tiles), 180-token chunks straddling row tiles,
+    chunks {0, 97, 98, 99}: far-apart frame positions."""
+    _check_fp4_recache(swl, Shapes(4, 128, 60, 3, 3, 6, 10), 99, 32, what="512-wide", q_rows=300)
+
+
+def test_recache_fp4_layer_full_size(swl):
+    """LongLive-1.3B layer: chunks {0, 1, 2, 3} = 18720 x 1536 hidden states
+    recached into an FP4 cache, then one 4680-query attention step.  The
+    encode checks cover sampled rows of every region (all of its codes are
+    compared bit for bit)."""
+    _check_fp4_recache(swl, LAYER_1P3B, 3, 33, rows=[0, 1, 51, 52, 1559, 1560, 3000, 4679],
+                       what="layer", q_rows=4680)
