@@ -19,12 +19,16 @@
 // cooperative launch -- and merges the pieces.  Without a workspace the shares
 // are whole items.
 //
-// Warp roles (320 threads; 448 with an FP4 cache):
+// Warp roles (320 threads; 512 with an FP4 cache):
 //   warps 0-3  softmax of slot 0 (thread i owns query row i: TMEM lane i)
 //   warps 4-7  softmax of slot 1
 //   warp  8    TMA producer: Q per piece, then K/V tiles through a 2-stage ring
 //   warp  9    TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 10-13 (FP4 cache only) dequantise K/V tiles into the smem ring
+//   FP4 cache only: warps 10-11 idle; warps 12-15 dequantise K/V tiles into
+//   the smem ring.  512 threads launch at 128 registers each; the warpgroups
+//   then split the register file with setmaxnreg: softmax 160 (the whole S row
+//   of a thread in registers, one pass), decode 112, TMA/MMA 80 -- per SM
+//   sub-partition 2 x 160 + 112 + 80 = 512, the launch's own share.
 // TMEM (512 columns): S0 [0,128) O0 [128,256) S1 [256,384) O1 [384,512);
 // P (bf16; f16 for FP4) overwrites the first 64 columns of S and feeds the
 // P*V MMA from TMEM.  The running max only moves when it grows by more than
@@ -46,7 +50,21 @@ constexpr int kStages = 2;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kDequantWarp0 = 10;
+constexpr int kDequantWarp0 = 12;  // FP4: warps 12-15 (warpgroup 3)
+// FP4 register split (setmaxnreg), per thread; must add up to the launch's
+// 128 per thread over the four warpgroups: 2 x 160 + 80 + 112 = 4 x 128.
+// (Of the splits that add up, this one leaves ptxas the fewest spills.)
+constexpr int kRegLaunch = 128;
+constexpr int kRegSoftmax = 160, kRegCtl = 80, kRegDecode = 112;
+static_assert(2 * kRegSoftmax + kRegCtl + kRegDecode == 4 * kRegLaunch, "register split");
+// setmaxnreg takes multiples of 8 in [24, 256]; .inc may only raise a warp's
+// count and .dec only lower it (anything else is an illegal instruction)
+static_assert(kRegSoftmax % 8 == 0 && kRegCtl % 8 == 0 && kRegDecode % 8 == 0, "setmaxnreg: multiple of 8");
+static_assert(kRegSoftmax > kRegLaunch && kRegSoftmax <= 256, "softmax warpgroups use setmaxnreg.inc");
+static_assert(kRegCtl < kRegLaunch && kRegCtl >= 24, "TMA/MMA warpgroup uses setmaxnreg.dec");
+static_assert(kRegDecode < kRegLaunch && kRegDecode >= 24, "decode warpgroup uses setmaxnreg.dec");
+template <bool kFp4>
+constexpr int attn_threads() { return kFp4 ? 512 : 320; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMinShareSteps = 8;          // K/V tiles per share at least (split-KV)
 
@@ -86,6 +104,9 @@ struct __align__(1024) AttnSmem {
   __nv_bfloat16 k[kStages][DB][BN * 64];
   __nv_bfloat16 v[kStages][DB][BN * 64];
   uint64_t bar_q, bar_qempty;
+  uint64_t bar_qcvt;       // FP4: Q rows converted to f16 (128 decode threads)
+  uint64_t bar_qread;      // FP4: every softmax thread holds its row's Q scale
+  float qinv[2][BM];       // FP4: per query row, 1 / its power-of-two f16 scale
   uint64_t bar_kfull[kStages], bar_kempty[kStages];
   uint64_t bar_vfull[kStages], bar_vempty[kStages];
   uint64_t bar_s[2], bar_p[2], bar_o[2], bar_ofree[2];
@@ -266,6 +287,45 @@ __device__ __forceinline__ void decode_row(__nv_bfloat16 (*dst)[BN * 64], int r,
   }
 }
 
+// FP4 cache: query row r of a Q tile (bf16, 128-byte swizzled) turned into
+// f16 in place, times 2^k with k chosen so the row's largest magnitude lies in
+// [2^14, 2^15): exact for every value that stays in the f16 normal range (a
+// bf16 value has 8 significant bits), which covers all but values below
+// 2^-28 of the row maximum.  Writes 2^-k (the factor the row's logits need).
+template <int D>
+__device__ __forceinline__ void convert_q_row(__nv_bfloat16 (*tile)[BM * 64], int r, float* inv_out) {
+  uint8_t* base = reinterpret_cast<uint8_t*>(tile);
+  auto at = [&](int c) -> uint4* {
+    return reinterpret_cast<uint4*>(base + (c >> 3) * (BM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  };
+  uint32_t mx = 0;  // largest |bf16| bit pattern of the row (monotone in the magnitude)
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 v = *at(c);
+    const uint32_t w[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0xFFFFu, w[e] >> 16));
+  }
+  int k = 0;  // zero, infinite or NaN rows keep scale 1
+  if (mx != 0 && mx < 0x7F80u) {
+    const int ex = (int)(mx >> 7) - 127;  // exponent field of the bf16 maximum, unbiased
+    k = min(126, max(-126, 14 - ex));
+  }
+  const float scale = __uint_as_float((uint32_t)(127 + k) << 23);
+  *inv_out = __uint_as_float((uint32_t)(127 - k) << 23);
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    uint4* a = at(c);
+    const uint4 v = *a;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * scale, __uint_as_float(w[e] & 0xFFFF0000u) * scale);
+    *a = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* a) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
@@ -276,7 +336,7 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long* a, unsign
 }
 
 template <int D, bool kFp4>
-__global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
+__global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
     sinkwin_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
@@ -292,6 +352,8 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_q, 1);
+    mbar_init(&sm.bar_qcvt, BN);
+    mbar_init(&sm.bar_qread, 2 * BM);
     mbar_init(&sm.bar_qempty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.bar_kfull[s], kvfull_count);
@@ -327,73 +389,214 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
   const uint32_t tmem = sm.tmem_base;
   const Watchdog wd{&sm.abort_flag, p.dev_err};
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      Share sh = share_of(p, g);
-      Piece pc;
-      uint32_t it = 0;  // K/V tiles of this CTA so far (ring position)
-      int npc = 0, nk = 0, nv = 0;
-      bool ok = true;
-      while (ok && sh.next(p, pc)) {
-        const int h = pc.u / p.n_pairs;
-        const int m0 = (pc.u % p.n_pairs) * (2 * BM);
-        const bool act1 = m0 + BM < p.tq;
-        if (npc > 0 && !mbar_wait(&sm.bar_qempty, (npc - 1) & 1, wd)) break;
-        mbar_expect_tx(&sm.bar_q, (act1 ? 2u : 1u) * DB * BM * 64 * 2);
-        for (int s = 0; s < (act1 ? 2 : 1); ++s)
-          for (int db = 0; db < DB; ++db)
-            tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
-        ++npc;
-        if (!kFp4) {
-          KvCursor cur;
-          cur.seek(p, Share::first_tile(p, pc));
-          const uint32_t tbytes = DB * BN * 64 * 2;
-          for (int t = pc.t0; t < pc.t1; ++t, ++it) {
-            const int st = it & 1, n = it >> 1;
-            if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(&sm.bar_kfull[st], tbytes);
+  if (warp >= kTmaWarp && warp < kTmaWarp + 4) {
+    // warpgroup 2: TMA producer, MMA issuer (FP4: two idle warps)
+    if constexpr (kFp4) setmaxnreg_dec<kRegCtl>();
+    if (warp == kTmaWarp) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        Share sh = share_of(p, g);
+        Piece pc;
+        uint32_t it = 0;  // K/V tiles of this CTA so far (ring position)
+        int npc = 0, nk = 0, nv = 0;
+        bool ok = true;
+        while (ok && sh.next(p, pc)) {
+          const int h = pc.u / p.n_pairs;
+          const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+          const bool act1 = m0 + BM < p.tq;
+          if (npc > 0 && !mbar_wait(&sm.bar_qempty, (npc - 1) & 1, wd)) break;
+          // FP4: the next Q (and its row scales) only once the softmax threads
+          // hold the previous piece's scales
+          if (kFp4 && npc > 0 && !mbar_wait(&sm.bar_qread, (npc - 1) & 1, wd)) break;
+          mbar_expect_tx(&sm.bar_q, (act1 ? 2u : 1u) * DB * BM * 64 * 2);
+          for (int s = 0; s < (act1 ? 2 : 1); ++s)
             for (int db = 0; db < DB; ++db)
-              tma_load_3d(&sm.k[st][db][0], &tmK, &sm.bar_kfull[st], db * 64, h, cur.row0(p));
-            ++nk;
-            if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
-              ok = false;
-              break;
+              tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
+          ++npc;
+          if (!kFp4) {
+            KvCursor cur;
+            cur.seek(p, Share::first_tile(p, pc));
+            const uint32_t tbytes = DB * BN * 64 * 2;
+            for (int t = pc.t0; t < pc.t1; ++t, ++it) {
+              const int st = it & 1, n = it >> 1;
+              if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(&sm.bar_kfull[st], tbytes);
+              for (int db = 0; db < DB; ++db)
+                tma_load_3d(&sm.k[st][db][0], &tmK, &sm.bar_kfull[st], db * 64, h, cur.row0(p));
+              ++nk;
+              if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(&sm.bar_vfull[st], tbytes);
+              for (int db = 0; db < DB; ++db)
+                tma_load_3d(&sm.v[st][db][0], &tmV, &sm.bar_vfull[st], db * 64, h, cur.row0(p));
+              ++nv;
+              cur.next(p);
             }
-            mbar_expect_tx(&sm.bar_vfull[st], tbytes);
-            for (int db = 0; db < DB; ++db)
-              tma_load_3d(&sm.v[st][db][0], &tmV, &sm.bar_vfull[st], db * 64, h, cur.row0(p));
-            ++nv;
-            cur.next(p);
           }
         }
-      }
-      // teardown after an abort: every copy this thread started must land
-      // before the CTA exits (the consumers waited for the rest)
-      if (sm.abort_flag) {
-        for (int st = 0; st < kStages; ++st) {
-          const int ck = nk > st ? (nk - st + 1) / 2 : 0;  // uses of stage st
-          const int cv = nv > st ? (nv - st + 1) / 2 : 0;
-          if (ck) mbar_drain(&sm.bar_kfull[st], (ck - 1) & 1);
-          if (cv) mbar_drain(&sm.bar_vfull[st], (cv - 1) & 1);
+        // teardown after an abort: every copy this thread started must land
+        // before the CTA exits (the consumers waited for the rest)
+        if (sm.abort_flag) {
+          for (int st = 0; st < kStages; ++st) {
+            const int ck = nk > st ? (nk - st + 1) / 2 : 0;  // uses of stage st
+            const int cv = nv > st ? (nv - st + 1) / 2 : 0;
+            if (ck) mbar_drain(&sm.bar_kfull[st], (ck - 1) & 1);
+            if (cv) mbar_drain(&sm.bar_vfull[st], (cv - 1) & 1);
+          }
+          if (npc) mbar_drain(&sm.bar_q, (npc - 1) & 1);
         }
-        if (npc) mbar_drain(&sm.bar_q, (npc - 1) & 1);
+      }
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        // FP4 cache: Q (converted in place) and K' are f16
+        constexpr uint32_t idesc_qk =
+            kFp4 ? idesc_f16_f32(BM, BN, false, false) : idesc_bf16_f32(BM, BN, false, false);
+        // FP4 cache: P (scaled by the V tensor scale) and V' are f16
+        constexpr uint32_t idesc_pv =
+            kFp4 ? idesc_f16_f32(BM, D, false, true) : idesc_bf16_f32(BM, D, false, true);
+        const uint32_t tS[2] = {tmem, tmem + 256};
+        const uint32_t tO[2] = {tmem + 128, tmem + 384};
+        // Descriptors: one base per operand, plus the slot / stage / k-step
+        // byte offset / 16 added right before each MMA with an opaque add, so
+        // the compiler keeps no table of precomputed descriptors alive.
+        const uint64_t qdesc = sdesc_sw128(smem_u32(&sm.q[0][0][0]), 0, 1024);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(&sm.k[0][0][0]), 0, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(&sm.v[0][0][0]), BN * 64 * 2, 1024);
+        constexpr uint32_t kDb16 = BM * 64 * 2 / 16;          // one 64-column block
+        constexpr uint32_t kQSlot16 = DB * kDb16;             // one query tile
+        constexpr uint32_t kKvStage16 = DB * BN * 64 * 2 / 16;  // one K or V stage
+        auto qk = [&](int slot, int st) {
+          const uint64_t qa = qdesc + slot * kQSlot16, kb = kdesc + st * kKvStage16;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kDb16 + (kk & 3) * 2;  // + 32 bytes per k-step
+            mma_bf16_ss(tS[slot], add_opaque(qa, off), add_opaque(kb, off), idesc_qk, kk > 0);
+          }
+        };
+        auto pv = [&](int slot, int st, bool acc) {
+          const uint64_t vb = vdesc + st * kKvStage16;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(tO[slot], tS[slot] + kk * 8, add_opaque(vb, kk * (2048 / 16)), idesc_pv,
+                        (acc || kk > 0) ? 1u : 0u);
+        };
+        Share sh = share_of(p, g);
+        Piece pc;
+        uint32_t it = 0;
+        int npc = 0;
+        int np[2] = {0, 0}, nof[2] = {0, 0};
+        bool pend[2] = {false, false};  // an epilogue of this slot may still read O
+        bool ok = true;
+        while (ok && sh.next(p, pc)) {
+          const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+          const bool act1 = m0 + BM < p.tq;
+          const int n = pc.t1 - pc.t0;
+          const int st0 = it & 1;
+          ok = mbar_wait(kFp4 ? &sm.bar_qcvt : &sm.bar_q, npc & 1, wd) &&
+               mbar_wait(&sm.bar_kfull[st0], (it >> 1) & 1, wd);
+          if (!ok) break;
+          tc_fence_after();
+          qk(0, st0);
+          mma_commit(&sm.bar_s[0]);
+          if (act1) {
+            qk(1, st0);
+            mma_commit(&sm.bar_s[1]);
+          }
+          mma_commit(&sm.bar_kempty[st0]);
+          if (n == 1) mma_commit(&sm.bar_qempty);
+          for (int i = 0; i < n && ok; ++i) {
+            const uint32_t ti = it + i;
+            const int st = ti & 1, ph = (ti >> 1) & 1;
+            const int nst = (ti + 1) & 1, nph = ((ti + 1) >> 1) & 1;
+            const bool more = i + 1 < n;
+            ok = mbar_wait(&sm.bar_p[0], np[0] & 1, wd) && mbar_wait(&sm.bar_vfull[st], ph, wd);
+            ++np[0];
+            if (ok && i == 0 && pend[0]) {
+              ok = mbar_wait(&sm.bar_ofree[0], nof[0] & 1, wd);
+              ++nof[0];
+              pend[0] = false;
+            }
+            if (!ok) break;
+            tc_fence_after();
+            pv(0, st, i > 0);
+            if (more) {
+              ok = mbar_wait(&sm.bar_kfull[nst], nph, wd);
+              if (!ok) break;
+              tc_fence_after();
+              qk(0, nst);
+              mma_commit(&sm.bar_s[0]);
+            } else {
+              mma_commit(&sm.bar_o[0]);
+            }
+            if (act1) {
+              ok = mbar_wait(&sm.bar_p[1], np[1] & 1, wd);
+              ++np[1];
+              if (ok && i == 0 && pend[1]) {
+                ok = mbar_wait(&sm.bar_ofree[1], nof[1] & 1, wd);
+                ++nof[1];
+                pend[1] = false;
+              }
+              if (!ok) break;
+              tc_fence_after();
+              pv(1, st, i > 0);
+              mma_commit(&sm.bar_vempty[st]);
+              if (more) {
+                qk(1, nst);
+                mma_commit(&sm.bar_s[1]);
+              } else {
+                mma_commit(&sm.bar_o[1]);
+              }
+            } else {
+              mma_commit(&sm.bar_vempty[st]);
+            }
+            if (more) mma_commit(&sm.bar_kempty[nst]);
+            if (i + 2 == n) mma_commit(&sm.bar_qempty);  // the piece's last QK went out above
+          }
+          it += n;
+          ++npc;
+          pend[0] = true;
+          if (act1) pend[1] = true;
+        }
+        // drain: every MMA issued above completes before TMEM is released
+        mma_commit(&sm.bar_drain);
+        mbar_drain(&sm.bar_drain, 0);
       }
     }
   } else if (kFp4 && warp >= kDequantWarp0) {
+    if constexpr (kFp4) setmaxnreg_dec<kRegDecode>();
     // ------------------------------------------------------------ FP4 dequant producer
     const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
     Share sh = share_of(p, g);
     Piece pc;
     uint32_t it = 0;
+    int npc = 0;
     bool ok = true;
     while (ok && sh.next(p, pc)) {
       const int h = pc.u / p.n_pairs;
+      // Q of the piece, once its TMA load landed: thread r turns query row r of
+      // each live slot into f16 in place, scaled by a power of two that puts
+      // the row's largest magnitude in [2^14, 2^15) (exact: a bf16 value has 8
+      // significant bits), and hands 1 / scale to that row's softmax thread
+      {
+        const int m0 = (pc.u % p.n_pairs) * (2 * BM);
+        const int nslot = m0 + BM < p.tq ? 2 : 1;
+        if (!mbar_wait(&sm.bar_q, npc & 1, wd)) break;
+        for (int sl = 0; sl < nslot; ++sl) convert_q_row<D>(sm.q[sl], r, &sm.qinv[sl][r]);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_qcvt);
+        ++npc;
+      }
       KvCursor cur;
       cur.seek(p, Share::first_tile(p, pc));
+      // One row of codes and scales per tensor in registers: the next tile's K
+      // row is loaded while this tile's V row decodes, and the next V row
+      // while the next K row decodes.
       RawRow<D> rk, rv;
       bool live = r < cur.valid(p);
       if (live) {
@@ -402,22 +605,17 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       }
       for (int t = pc.t0; t < pc.t1; ++t, ++it) {
         const int st = it & 1, n = it >> 1;
-        // the next tile's codes and scales are in flight while this one decodes
         KvCursor nxt = cur;
         nxt.next(p);
-        RawRow<D> nk, nv;
         const bool nlive = t + 1 < pc.t1 && r < nxt.valid(p);
-        if (nlive) {
-          load_raw<D>(nk, p.kc, p.ks, nxt.row0(p) + r, p, h);
-          load_raw<D>(nv, p.vc, p.vs, nxt.row0(p) + r, p, h);
-        }
         if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
           ok = false;
           break;
         }
-        decode_row<D, false>(sm.k[st], r, live, rk);
+        decode_row<D, true>(sm.k[st], r, live, rk);
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_kfull[st]);
+        if (nlive) load_raw<D>(rk, p.kc, p.ks, nxt.row0(p) + r, p, h);  // in flight during V
         if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
           ok = false;
           break;
@@ -425,119 +623,13 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
         decode_row<D, true>(sm.v[st], r, live, rv);
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_vfull[st]);
-        rk = nk;
-        rv = nv;
+        if (nlive) load_raw<D>(rv, p.vc, p.vs, nxt.row0(p) + r, p, h);  // in flight during K
         live = nlive;
         cur = nxt;
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-      // FP4 cache: P (scaled by the V tensor scale) and V' are f16
-      constexpr uint32_t idesc_pv =
-          kFp4 ? idesc_f16_f32(BM, D, false, true) : idesc_bf16_f32(BM, D, false, true);
-      const uint32_t tS[2] = {tmem, tmem + 256};
-      const uint32_t tO[2] = {tmem + 128, tmem + 384};
-      auto qk = [&](int slot, int st) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(smem_u32(&sm.q[slot][kk >> 2][0]) + koff, 0, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(&sm.k[st][kk >> 2][0]) + koff, 0, 1024);
-          mma_bf16_ss(tS[slot], ad, bd, idesc_qk, kk > 0);
-        }
-      };
-      auto pv = [&](int slot, int st, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(smem_u32(&sm.v[st][0][0]) + kk * 2048, BN * 64 * 2, 1024);
-          mma_bf16_ts(tO[slot], tS[slot] + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      Share sh = share_of(p, g);
-      Piece pc;
-      uint32_t it = 0;
-      int npc = 0;
-      int np[2] = {0, 0}, nof[2] = {0, 0};
-      bool pend[2] = {false, false};  // an epilogue of this slot may still read O
-      bool ok = true;
-      while (ok && sh.next(p, pc)) {
-        const int m0 = (pc.u % p.n_pairs) * (2 * BM);
-        const bool act1 = m0 + BM < p.tq;
-        const int n = pc.t1 - pc.t0;
-        const int st0 = it & 1;
-        ok = mbar_wait(&sm.bar_q, npc & 1, wd) && mbar_wait(&sm.bar_kfull[st0], (it >> 1) & 1, wd);
-        if (!ok) break;
-        tc_fence_after();
-        qk(0, st0);
-        mma_commit(&sm.bar_s[0]);
-        if (act1) {
-          qk(1, st0);
-          mma_commit(&sm.bar_s[1]);
-        }
-        mma_commit(&sm.bar_kempty[st0]);
-        if (n == 1) mma_commit(&sm.bar_qempty);
-        for (int i = 0; i < n && ok; ++i) {
-          const uint32_t ti = it + i;
-          const int st = ti & 1, ph = (ti >> 1) & 1;
-          const int nst = (ti + 1) & 1, nph = ((ti + 1) >> 1) & 1;
-          const bool more = i + 1 < n;
-          ok = mbar_wait(&sm.bar_p[0], np[0] & 1, wd) && mbar_wait(&sm.bar_vfull[st], ph, wd);
-          ++np[0];
-          if (ok && i == 0 && pend[0]) {
-            ok = mbar_wait(&sm.bar_ofree[0], nof[0] & 1, wd);
-            ++nof[0];
-            pend[0] = false;
-          }
-          if (!ok) break;
-          tc_fence_after();
-          pv(0, st, i > 0);
-          if (more) {
-            ok = mbar_wait(&sm.bar_kfull[nst], nph, wd);
-            if (!ok) break;
-            tc_fence_after();
-            qk(0, nst);
-            mma_commit(&sm.bar_s[0]);
-          } else {
-            mma_commit(&sm.bar_o[0]);
-          }
-          if (act1) {
-            ok = mbar_wait(&sm.bar_p[1], np[1] & 1, wd);
-            ++np[1];
-            if (ok && i == 0 && pend[1]) {
-              ok = mbar_wait(&sm.bar_ofree[1], nof[1] & 1, wd);
-              ++nof[1];
-              pend[1] = false;
-            }
-            if (!ok) break;
-            tc_fence_after();
-            pv(1, st, i > 0);
-            mma_commit(&sm.bar_vempty[st]);
-            if (more) {
-              qk(1, nst);
-              mma_commit(&sm.bar_s[1]);
-            } else {
-              mma_commit(&sm.bar_o[1]);
-            }
-          } else {
-            mma_commit(&sm.bar_vempty[st]);
-          }
-          if (more) mma_commit(&sm.bar_kempty[nst]);
-          if (i + 2 == n) mma_commit(&sm.bar_qempty);  // the piece's last QK went out above
-        }
-        it += n;
-        ++npc;
-        pend[0] = true;
-        if (act1) pend[1] = true;
-      }
-      // drain: every MMA issued above completes before TMEM is released
-      mma_commit(&sm.bar_drain);
-      mbar_drain(&sm.bar_drain, 0);
-    }
   } else if (warp < kSoftmaxWarps) {
+    if constexpr (kFp4) setmaxnreg_inc<kRegSoftmax>();
     // ------------------------------------------------------------ softmax
     const int slot = warp >> 2;
     const int wq = warp & 3;
@@ -550,6 +642,7 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
     Piece pc;
     uint32_t it = 0;
     int ns = 0, no = 0;
+    [[maybe_unused]] int nq = 0;  // FP4: converted-Q phases waited
     bool ok = true;
     int kv_region = -1;  // FP4: region whose tensor scales are held below
     float kv_kg = 0.0f, kv_vg = 0.0f;
@@ -575,6 +668,18 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
       const int n = pc.t1 - pc.t0;
       const uint32_t it0 = it;
       it += n;
+      [[maybe_unused]] float qinv = 1.0f;
+      if constexpr (kFp4) {
+        // every piece converts Q once (both slots' rows in the same phase)
+        const bool got = mbar_wait(&sm.bar_qcvt, nq & 1, wd);
+        ++nq;
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        qinv = sm.qinv[slot][row];
+        mbar_arrive(&sm.bar_qread);  // the decode warps may overwrite qinv from now on
+      }
       if (slot == 1 && !act1) continue;
       float m_ref = -INFINITY, l = 0.0f;
       // Keep a stale running max unless it grew by more than 2^8.  decide()
@@ -635,115 +740,72 @@ __global__ void __launch_bounds__(kFp4 ? 448 : 320, 1)
           }
           fence_proxy_async_smem();
         }
-        if constexpr (!kFp4) {
-          // one pass: the whole S row lives in registers
-          uint32_t sr[BN];
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j)
-            tmem_ld32(tS + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[j * 32]));
-          tmem_ld_wait();
-          if (valid < BN) {  // ragged tile (warp-uniform): keys past the end do not count
-#pragma unroll
-            for (int j = 0; j < BN; ++j)
-              if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
-          }
-          // row max: four independent 3-input max chains
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int j = 0; j < BN; j += 8)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              m4[q] = fmax3(m4[q], __uint_as_float(sr[j + 2 * q]), __uint_as_float(sr[j + 2 * q + 1]));
-          const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-          const float alpha = decide(i, mx * c);
-          // p = 2^(s*c - m): one packed FFMA per pair, packed row sum, bf16 pairs
-          // written back over the consumed S columns
-          const uint64_t c2 = f32x2(c, c), n2 = f32x2(-m_ref, -m_ref);
-          uint64_t acc2 = f32x2(0.0f, 0.0f);
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const uint64_t y2 = ffma2(f32x2(__uint_as_float(sr[j * 64 + 2 * e]),
-                                              __uint_as_float(sr[j * 64 + 2 * e + 1])), c2, n2);
-              float y0, y1;
-              f32x2_split(y2, y0, y1);
-              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-              acc2 = fadd2(acc2, f32x2(p0, p1));
-              pk[e] = pack_bf16x2(p0, p1);
-            }
-            tmem_st32(tS + j * 32, pk);
-          }
-          float s0, s1;
-          f32x2_split(acc2, s0, s1);
-          l += s0 + s1;
-          apply(alpha);
-        } else {
-          // two passes over 32-column chunks (fewer live registers).  The tile
-          // lies in one region: its K tensor scale joins the logit scale, its
-          // V tensor scale multiplies P (stored as f16 for the f16 P*V MMA)
+        // one pass: the whole S row lives in registers.  FP4: the tile lies in
+        // one region; its K tensor scale joins the logit scale and its V
+        // tensor scale multiplies P (stored as f16 for the f16 P*V MMA)
+        float cg = c;
+        [[maybe_unused]] float gv = 1.0f;
+        if constexpr (kFp4) {
           const int region = p.seg_region[cur.seg];
           if (region != kv_region) {  // consecutive tiles mostly share a region
             kv_region = region;
             kv_kg = __ldg(p.kg + region);
             kv_vg = __ldg(p.vg + region) * inv_v_shift;
           }
-          const float cg = c * kv_kg;
-          const float gv = kv_vg;
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j) {
-            uint32_t sr[32];
-            tmem_ld32(tS + j * 32, sr);
-            tmem_ld_wait();
-            if (valid < BN) {  // ragged tile (warp-uniform)
+          cg = c * kv_kg * qinv;
+          gv = kv_vg;
+        }
+        uint32_t sr[BN];
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (j * 32 + e >= valid) sr[e] = __float_as_uint(-INFINITY);
-            }
+        for (int j = 0; j < BN / 32; ++j)
+          tmem_ld32(tS + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[j * 32]));
+        tmem_ld_wait();
+        if (valid < BN) {  // ragged tile (warp-uniform): keys past the end do not count
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
+          for (int j = 0; j < BN; ++j)
+            if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+        }
+        // row max: four independent 3-input max chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                m4[q] = fmax3(m4[q], __uint_as_float(sr[e + 2 * q]), __uint_as_float(sr[e + 2 * q + 1]));
-          }
-          const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-          const float alpha = decide(i, mx * cg);
-          const uint64_t c2 = f32x2(cg, cg), n2 = f32x2(-m_ref, -m_ref), g2 = f32x2(gv, gv);
-          uint64_t acc2 = f32x2(0.0f, 0.0f);
-#pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j) {
-            // chunk j (keys 32j..32j+31) -> P columns 16j..16j+15, which only
-            // overlap S columns already consumed
-            uint32_t sr[32];
-            tmem_ld32(tS + j * 32, sr);
-            tmem_ld_wait();
-            if (valid < BN) {
+        for (int j = 0; j < BN; j += 8)
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (j * 32 + e >= valid) sr[e] = __float_as_uint(-INFINITY);
-            }
-            uint32_t pk[16];
+          for (int q = 0; q < 4; ++q)
+            m4[q] = fmax3(m4[q], __uint_as_float(sr[j + 2 * q]), __uint_as_float(sr[j + 2 * q + 1]));
+        const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+        const float alpha = decide(i, mx * cg);
+        // p = 2^(s*cg - m): one packed FFMA per pair, packed row sum; pairs
+        // (bf16, or f16 times the V tensor scale) written back over the
+        // consumed S columns
+        const uint64_t c2 = f32x2(cg, cg), n2 = f32x2(-m_ref, -m_ref);
+        [[maybe_unused]] const uint64_t g2 = f32x2(gv, gv);
+        uint64_t acc2 = f32x2(0.0f, 0.0f);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const uint64_t y2 =
-                  ffma2(f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2, n2);
-              float y0, y1;
-              f32x2_split(y2, y0, y1);
-              const uint64_t p2 = f32x2(ex2_approx(y0), ex2_approx(y1));
-              acc2 = fadd2(acc2, p2);
+        for (int j = 0; j < BN / 64; ++j) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint64_t y2 = ffma2(f32x2(__uint_as_float(sr[j * 64 + 2 * e]),
+                                            __uint_as_float(sr[j * 64 + 2 * e + 1])), c2, n2);
+            float y0, y1;
+            f32x2_split(y2, y0, y1);
+            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            const uint64_t p2 = f32x2(p0, p1);
+            acc2 = fadd2(acc2, p2);
+            if constexpr (kFp4) {
               float q0, q1;
               f32x2_split(fmul2(p2, g2), q0, q1);
               pk[e] = pack_f16x2(q0, q1);
+            } else {
+              pk[e] = pack_bf16x2(p0, p1);
             }
-            tmem_st16(tS + j * 16, pk);
           }
-          float s0, s1;
-          f32x2_split(acc2, s0, s1);
-          l += s0 + s1;
-          apply(alpha);
+          tmem_st32(tS + j * 32, pk);
         }
+        float s0, s1;
+        f32x2_split(acc2, s0, s1);
+        l += s0 + s1;
+        apply(alpha);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.bar_p[slot]);
@@ -955,9 +1017,24 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   static bool smem_set[64] = {};  // one per instantiation of this launcher
   cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
+  if constexpr (kFp4) {
+    // the setmaxnreg split hands out exactly the registers the block launches
+    // with: refuse to launch if the compiled kernel's count differs (an
+    // increase that the launch cannot cover would wait forever)
+    static int regs_ok[64] = {};  // per device: 0 unknown, 1 ok, -1 mismatch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (regs_ok[dev] == 0) {
+      cudaFuncAttributes fa{};
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      regs_ok[dev] = fa.numRegs == kRegLaunch ? 1 : -1;
+    }
+    if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.G, 1, 1);
-  cfg.blockDim = dim3(kFp4 ? 448 : 320, 1, 1);
+  cfg.blockDim = dim3(attn_threads<kFp4>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   // a merge waits on a neighbouring CTA: all CTAs must be resident together

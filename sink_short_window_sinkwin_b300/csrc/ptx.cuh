@@ -219,6 +219,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// a + b in a form the compiler neither folds nor hoists (descriptor offsets
+// computed right where they are used)
+__device__ __forceinline__ uint64_t add_opaque(uint64_t a, uint32_t b) {
+  uint64_t r;
+  asm volatile("add.u64 %0, %1, %2;" : "=l"(r) : "l"(a), "l"((uint64_t)b));
+  return r;
+}
+
 // tcgen05.ld / st, 32 lanes x 32 bit, 32 consecutive columns per thread
 #define KVC_R32(r)                                                                              \
   "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),          \
@@ -310,6 +318,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Register split between warpgroups (all four warps of a warpgroup execute
+// the same one).  inc blocks until the registers are free, so the new counts
+// of all warpgroups must add up to no more than the launch's own.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Programmatic dependent launch.  launch_dependents: the next grid in the
