@@ -27,8 +27,8 @@
 //   FP4 cache only: warps 10-11 idle; warps 12-15 dequantise K/V tiles into
 //   the smem ring.  512 threads launch at 128 registers each; the warpgroups
 //   then split the register file with setmaxnreg: softmax 160 (the whole S row
-//   of a thread in registers, one pass), decode 112, TMA/MMA 80 -- per SM
-//   sub-partition 2 x 160 + 112 + 80 = 512, the launch's own share.
+//   of a thread in registers, one pass), decode 104, TMA/MMA 72 -- per SM
+//   sub-partition 2 x 168 + 104 + 72 = 512, the launch's own share.
 // TMEM (512 columns): S0 [0,128) O0 [128,256) S1 [256,384) O1 [384,512);
 // P (bf16; f16 for FP4) overwrites the first 64 columns of S and feeds the
 // P*V MMA from TMEM.  The running max only moves when it grows by more than
@@ -52,10 +52,10 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDequantWarp0 = 12;  // FP4: warps 12-15 (warpgroup 3)
 // FP4 register split (setmaxnreg), per thread; must add up to the launch's
-// 128 per thread over the four warpgroups: 2 x 160 + 80 + 112 = 4 x 128.
+// 128 per thread over the four warpgroups: 2 x 168 + 72 + 104 = 4 x 128.
 // (Of the splits that add up, this one leaves ptxas the fewest spills.)
 constexpr int kRegLaunch = 128;
-constexpr int kRegSoftmax = 160, kRegCtl = 80, kRegDecode = 112;
+constexpr int kRegSoftmax = 168, kRegCtl = 72, kRegDecode = 104;
 static_assert(2 * kRegSoftmax + kRegCtl + kRegDecode == 4 * kRegLaunch, "register split");
 // setmaxnreg takes multiples of 8 in [24, 256]; .inc may only raise a warp's
 // count and .dec only lower it (anything else is an illegal instruction)
@@ -114,6 +114,23 @@ struct __align__(1024) AttnSmem {
   uint64_t bar_drain;
   uint32_t tmem_base;
   int32_t abort_flag;
+};
+
+// FP4 cache: the decode warps' own prefetch ring of raw rows (codes and block
+// scales), filled by per-thread cp.async copies.  Items alternate K and V of
+// consecutive tiles and take slots 0, 1, 2, 0, ...; thread r owns row r of
+// each slot.  A row's 16-byte code chunks are XOR-swizzled so that the eight
+// threads of a quarter-warp read eight different bank groups.
+template <int D>
+struct __align__(16) RawRing {
+  static constexpr int kSlots = 3;
+  static constexpr int kNch = D / 32;                   // 16-byte code chunks of a row
+  static constexpr int kShift = D == 128 ? 1 : 2;       // log2(rows per 128-byte line)
+  uint8_t codes[kSlots][BN * (D / 2)];
+  uint8_t scales[kSlots][BN * (D / 16)];
+  __device__ __forceinline__ static int chunk_off(int r, int q) {
+    return r * (D / 2) + ((q ^ ((r >> kShift) & (kNch - 1))) << 4);
+  }
 };
 
 // K/V tile cursor over the visible segments.
@@ -572,6 +589,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
     if constexpr (kFp4) setmaxnreg_dec<kRegDecode>();
     // ------------------------------------------------------------ FP4 dequant producer
     const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
+    RawRing<D>& raw = *reinterpret_cast<RawRing<D>*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(Smem));
     Share sh = share_of(p, g);
     Piece pc;
     uint32_t it = 0;
@@ -592,42 +610,68 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
         mbar_arrive(&sm.bar_qcvt);
         ++npc;
       }
-      KvCursor cur;
+      // Items j = 0, 1, ... of the piece are K (even j) and V (odd j) of its
+      // tiles in turn; item j's raw row is copied into slot j % 3 three items
+      // ahead of its decode, so it has had a tile and a half to land.
+      KvCursor cur, icur;  // tile being decoded / tile of the next item to copy
       cur.seek(p, Share::first_tile(p, pc));
-      // One row of codes and scales per tensor in registers: the next tile's K
-      // row is loaded while this tile's V row decodes, and the next V row
-      // while the next K row decodes.
-      RawRow<D> rk, rv;
-      bool live = r < cur.valid(p);
-      if (live) {
-        load_raw<D>(rk, p.kc, p.ks, cur.row0(p) + r, p, h);
-        load_raw<D>(rv, p.vc, p.vs, cur.row0(p) + r, p, h);
-      }
-      for (int t = pc.t0; t < pc.t1; ++t, ++it) {
-        const int st = it & 1, n = it >> 1;
-        KvCursor nxt = cur;
-        nxt.next(p);
-        const bool nlive = t + 1 < pc.t1 && r < nxt.valid(p);
-        if (it >= kStages && !mbar_wait(&sm.bar_kempty[st], (n - 1) & 1, wd)) {
+      icur = cur;
+      const int nitems = 2 * (pc.t1 - pc.t0);
+      int issued = 0, islot = 0;
+      auto issue = [&]() {
+        const bool isv = issued & 1;
+        if (r < icur.valid(p)) {
+          const size_t row = (size_t)(icur.row0(p) + r) * p.H + h;
+          const uint8_t* cs = (isv ? p.vc : p.kc) + row * (D / 2);
+          const uint8_t* ss = (isv ? p.vs : p.ks) + row * (D / 16);
+#pragma unroll
+          for (int q = 0; q < RawRing<D>::kNch; ++q) cp_async_16(raw.codes[islot] + RawRing<D>::chunk_off(r, q), cs + 16 * q);
+          if constexpr (D == 128) cp_async_8(raw.scales[islot] + r * 8, ss);
+          else cp_async_4(raw.scales[islot] + r * 4, ss);
+        }
+        cp_async_commit();  // one group per item, empty for a row past the tile's end
+        if (isv) icur.next(p);
+        ++issued;
+        islot = islot == 2 ? 0 : islot + 1;
+      };
+      for (int k = 0; k < 3 && k < nitems; ++k) issue();
+      for (int j = 0; j < nitems; ++j) {
+        const bool isv = j & 1;
+        const uint32_t ti = it + (j >> 1);
+        const int st = ti & 1, n = ti >> 1;
+        const int pending = issued - 1 - j;  // items copied after this one
+        if (pending >= 2) cp_async_wait<2>();
+        else if (pending == 1) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        uint64_t* empty = isv ? &sm.bar_vempty[st] : &sm.bar_kempty[st];
+        if (ti >= kStages && !mbar_wait(empty, (n - 1) & 1, wd)) {
           ok = false;
           break;
         }
-        decode_row<D, true>(sm.k[st], r, live, rk);
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.bar_kfull[st]);
-        if (nlive) load_raw<D>(rk, p.kc, p.ks, nxt.row0(p) + r, p, h);  // in flight during V
-        if (it >= kStages && !mbar_wait(&sm.bar_vempty[st], (n - 1) & 1, wd)) {
-          ok = false;
-          break;
+        const bool live = r < cur.valid(p);
+        RawRow<D> rw;
+        if (live) {
+          const int sl = j % 3;
+#pragma unroll
+          for (int q = 0; q < RawRing<D>::kNch; ++q)
+            rw.c[q] = *reinterpret_cast<const uint4*>(raw.codes[sl] + RawRing<D>::chunk_off(r, q));
+          if constexpr (D == 128) {
+            const uint2 s8 = *reinterpret_cast<const uint2*>(raw.scales[sl] + r * 8);
+            rw.s[0] = s8.x;
+            rw.s[1] = s8.y;
+          } else {
+            rw.s[0] = *reinterpret_cast<const uint32_t*>(raw.scales[sl] + r * 4);
+          }
         }
-        decode_row<D, true>(sm.v[st], r, live, rv);
+        decode_row<D, true>(isv ? sm.v[st] : sm.k[st], r, live, rw);
         fence_proxy_async_smem();
-        mbar_arrive(&sm.bar_vfull[st]);
-        if (nlive) load_raw<D>(rv, p.vc, p.vs, nxt.row0(p) + r, p, h);  // in flight during K
-        live = nlive;
-        cur = nxt;
+        mbar_arrive(isv ? &sm.bar_vfull[st] : &sm.bar_kfull[st]);
+        if (isv) cur.next(p);
+        if (issued < nitems) issue();  // into the slot just read
       }
+      it += pc.t1 - pc.t0;
     }
+    cp_async_wait<0>();  // no copy into this CTA's shared memory outlives it
   } else if (warp < kSoftmaxWarps) {
     if constexpr (kFp4) setmaxnreg_inc<kRegSoftmax>();
     // ------------------------------------------------------------ softmax
@@ -1011,7 +1055,7 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   }
   // one CTA per SM: a second resident CTA would wait in tcgen05.alloc for the
   // 512 TMEM columns the first one holds
-  size_t smem = sizeof(AttnSmem<D>) + 1024;
+  size_t smem = sizeof(AttnSmem<D>) + (kFp4 ? sizeof(RawRing<D>) : 0) + 1024;
   if (smem < 120 * 1024) smem = 120 * 1024;
   auto kern = sinkwin_attn_kernel<D, kFp4>;
   static bool smem_set[64] = {};  // one per instantiation of this launcher
