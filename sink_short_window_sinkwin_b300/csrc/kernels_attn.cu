@@ -51,20 +51,36 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDequantWarp0 = 12;  // FP4: warps 12-15 (warpgroup 3)
-// FP4 register split (setmaxnreg), per thread; must add up to the launch's
-// 128 per thread over the four warpgroups: 2 x 168 + 72 + 104 = 4 x 128.
-// (Of the splits that add up, this one leaves ptxas the fewest spills.)
-constexpr int kRegLaunch = 128;
-constexpr int kRegSoftmax = 168, kRegCtl = 72, kRegDecode = 104;
-static_assert(2 * kRegSoftmax + kRegCtl + kRegDecode == 4 * kRegLaunch, "register split");
-// setmaxnreg takes multiples of 8 in [24, 256]; .inc may only raise a warp's
-// count and .dec only lower it (anything else is an illegal instruction)
-static_assert(kRegSoftmax % 8 == 0 && kRegCtl % 8 == 0 && kRegDecode % 8 == 0, "setmaxnreg: multiple of 8");
-static_assert(kRegSoftmax > kRegLaunch && kRegSoftmax <= 256, "softmax warpgroups use setmaxnreg.inc");
-static_assert(kRegCtl < kRegLaunch && kRegCtl >= 24, "TMA/MMA warpgroup uses setmaxnreg.dec");
-static_assert(kRegDecode < kRegLaunch && kRegDecode >= 24, "decode warpgroup uses setmaxnreg.dec");
+// FP4 warpgroup register split (setmaxnreg), per thread.  The block launches
+// with kLaunch registers a thread (the launch-bounds maximum, which ptxas takes
+// when setmaxnreg is present; the launcher checks it), and the new counts of
+// all warps must add up to exactly that budget:
+//   16 warps at 128: softmax 8 x 168 + TMA/MMA/idle 4 x 72 + decode 4 x 104 = 16 x 128
+// and per SM sub-partition (one warp of each warpgroup) at most 512.  The bf16
+// kernel (10 warps, no split) runs at the 168 its launch allows.
 template <bool kFp4>
-constexpr int attn_threads() { return kFp4 ? 512 : 320; }
+struct RegSplit;
+template <>
+struct RegSplit<false> {
+  static constexpr int kThreads = 320;
+};
+template <>
+struct RegSplit<true> {
+  static constexpr int kThreads = 512, kLaunch = 128, kSoftmax = 168, kCtl = 72, kDecode = 104;
+};
+constexpr bool fp4_split_ok() {
+  using R = RegSplit<true>;
+  return 8 * R::kSoftmax + 4 * R::kCtl + 4 * R::kDecode == (R::kThreads / 32) * R::kLaunch &&
+         2 * R::kSoftmax + R::kCtl + R::kDecode <= 512 &&
+         // setmaxnreg takes multiples of 8 in [24, 256]; .inc may only raise a
+         // warp's count and .dec only lower it (else: an illegal instruction)
+         R::kSoftmax % 8 == 0 && R::kCtl % 8 == 0 && R::kDecode % 8 == 0 &&
+         R::kSoftmax > R::kLaunch && R::kSoftmax <= 256 && R::kCtl < R::kLaunch && R::kCtl >= 24 &&
+         R::kDecode < R::kLaunch && R::kDecode >= 24 && 65536 / R::kThreads / 8 * 8 == R::kLaunch;
+}
+static_assert(fp4_split_ok(), "register split");
+template <bool kFp4>
+constexpr int attn_threads() { return RegSplit<kFp4>::kThreads; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMinShareSteps = 8;          // K/V tiles per share at least (split-KV)
 
@@ -408,7 +424,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
 
   if (warp >= kTmaWarp && warp < kTmaWarp + 4) {
     // warpgroup 2: TMA producer, MMA issuer (FP4: two idle warps)
-    if constexpr (kFp4) setmaxnreg_dec<kRegCtl>();
+    if constexpr (kFp4) setmaxnreg_dec<RegSplit<true>::kCtl>();
     if (warp == kTmaWarp) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -480,8 +496,9 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
         const uint32_t tS[2] = {tmem, tmem + 256};
         const uint32_t tO[2] = {tmem + 128, tmem + 384};
         // Descriptors: one base per operand, plus the slot / stage / k-step
-        // byte offset / 16 added right before each MMA with an opaque add, so
-        // the compiler keeps no table of precomputed descriptors alive.
+        // byte offset / 16.  FP4 (72-register control warps): added right
+        // before each MMA with an opaque add, so the compiler keeps no table
+        // of precomputed descriptors alive.
         const uint64_t qdesc = sdesc_sw128(smem_u32(&sm.q[0][0][0]), 0, 1024);
         const uint64_t kdesc = sdesc_sw128(smem_u32(&sm.k[0][0][0]), 0, 1024);
         const uint64_t vdesc = sdesc_sw128(smem_u32(&sm.v[0][0][0]), BN * 64 * 2, 1024);
@@ -493,15 +510,19 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kDb16 + (kk & 3) * 2;  // + 32 bytes per k-step
-            mma_bf16_ss(tS[slot], add_opaque(qa, off), add_opaque(kb, off), idesc_qk, kk > 0);
+            if constexpr (kFp4)
+              mma_bf16_ss(tS[slot], add_opaque(qa, off), add_opaque(kb, off), idesc_qk, kk > 0);
+            else
+              mma_bf16_ss(tS[slot], qa + off, kb + off, idesc_qk, kk > 0);
           }
         };
         auto pv = [&](int slot, int st, bool acc) {
           const uint64_t vb = vdesc + st * kKvStage16;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tO[slot], tS[slot] + kk * 8, add_opaque(vb, kk * (2048 / 16)), idesc_pv,
-                        (acc || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = kFp4 ? add_opaque(vb, kk * (2048 / 16)) : vb + kk * (2048 / 16);
+            mma_bf16_ts(tO[slot], tS[slot] + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          }
         };
         Share sh = share_of(p, g);
         Piece pc;
@@ -586,7 +607,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
       }
     }
   } else if (kFp4 && warp >= kDequantWarp0) {
-    if constexpr (kFp4) setmaxnreg_dec<kRegDecode>();
+    if constexpr (kFp4) setmaxnreg_dec<RegSplit<true>::kDecode>();
     // ------------------------------------------------------------ FP4 dequant producer
     const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
     RawRing<D>& raw = *reinterpret_cast<RawRing<D>*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(Smem));
@@ -673,7 +694,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
     }
     cp_async_wait<0>();  // no copy into this CTA's shared memory outlives it
   } else if (warp < kSoftmaxWarps) {
-    if constexpr (kFp4) setmaxnreg_inc<kRegSoftmax>();
+    if constexpr (kFp4) setmaxnreg_inc<RegSplit<true>::kSoftmax>();
     // ------------------------------------------------------------ softmax
     const int slot = warp >> 2;
     const int wq = warp & 3;
@@ -1072,7 +1093,7 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
       cudaFuncAttributes fa{};
       e = cudaFuncGetAttributes(&fa, kern);
       if (e != cudaSuccess) return e;
-      regs_ok[dev] = fa.numRegs == kRegLaunch ? 1 : -1;
+      regs_ok[dev] = fa.numRegs == RegSplit<true>::kLaunch ? 1 : -1;
     }
     if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
   }
