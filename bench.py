@@ -5,7 +5,9 @@ x 128, a 4680-query chunk of 3 frames against 18720 cached keys: 1 sink chunk +
 3 window slots): TFLOP/s, latent frames/s per layer and % of the bf16 dense
 peak.  It is measured inside one step of the whole path:
     recache   [K|V] = Hid(18720x1536) @ W_kv(1536x3072), RMSNorm + 3D RoPE -> cache
-    bf16      evict oldest chunk, append the new chunk, attention of its 4680 queries
+    bf16      evict oldest chunk, project the new chunk ([Q|K|V] = Hid(4680x1536) @
+              W(1536x4608), Q/K RMSNorm + 3D RoPE, K/V straight into the ring slot),
+              attention of its 4680 queries
     fp4       evict, append (FP4 encode), attention with fused dequantisation
 Steps rotate over 8 independent layer caches, so every step touches > 126 MB
 (larger than L2) that the previous step did not.  A second leg streams 30
@@ -39,7 +41,8 @@ LK = (1 + W) * TC        # 18720 visible keys at steady state
 HD = H * D
 ATTN_FLOP = 4.0 * H * TC * LK * D          # QK^T + PV, 538.27 GFLOP
 RECACHE_FLOP = 2.0 * LK * HD * (2 * HD)    # 176.66 GFLOP
-STEP_FLOP = 2 * ATTN_FLOP + RECACHE_FLOP
+PROJECT_FLOP = 2.0 * TC * HD * (3 * HD)    # 66.25 GFLOP: one chunk's [Q|K|V] projection
+STEP_FLOP = 2 * ATTN_FLOP + RECACHE_FLOP + PROJECT_FLOP
 NLAYERS = 8
 # algorithmic bytes per launch (read + write of the data the operation must touch)
 APPEND_BF16_BYTES = 2 * 2 * TC * HD * 2                         # read K,V chunk + write cache
@@ -55,8 +58,12 @@ WORKLOAD = ("LongLive-1.3B layer chunk step: 12 heads x 128, 4680 queries/chunk,
 TRAFFIC = {
     # ncu --set full on the LongLive-1.3B layer workload (one launch each);
     # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
-    "sinkwin_attn_kernel<128,false>": {"bytes": 309258240 + 26184960, "src_sha": "e2953c2cbf9151d6"},
-    "sinkwin_attn_kernel<128,true>": {"bytes": 48115200 + 4129024, "src_sha": "e2953c2cbf9151d6"},
+    "sinkwin_attn_kernel<128,false>": {"bytes": 305278720 + 26565120, "src_sha": "b4ae518685bd2dfc"},
+    "sinkwin_attn_kernel<128,true>": {"bytes": 47181056 + 4062208, "src_sha": "b4ae518685bd2dfc"},
+    # K GEMM + norm + V GEMM of one recache; profiles/recache_gemm_layer1p3b.md
+    "recache_gemm_kernel<256,*> x2 + recache_norm_rope_kernel": {
+        "bytes": (62334208 + 60034048) + (115096064 + 15608320) + (62250752 + 19588608),
+        "src_sha": "c2165c20461392cd"},
 }
 
 
@@ -262,6 +269,70 @@ def hbm_kernels(swl, dev, layers, randn, per_graph: int = 8, replays: int = 6):
 
 
 # ---------------------------------------------------------------------------
+# Further rows of the path, timed on their own (CUDA events, median of runs)
+# ---------------------------------------------------------------------------
+def extra_rows(swl, dev, randn, wkv, wqkv, gamma, runs: int = 12):
+    """Split-KV attention of short query chunks (with and without the merge
+    workspace), the recache into an FP4 cache, and the chunk projection into an
+    FP4 cache.  Work rotates over two caches (> L2 together)."""
+    import torch
+    scale = 1.0 / math.sqrt(D)
+
+    def med(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(runs)]
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            a.record()
+            fn(i)
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    def filled(dt, **kw):
+        c = swl.KVCache(H, D, TPF, CF, W, dtype=dt, device=dev, **kw)
+        for ch in range(1 + W):
+            c.append(randn((TC, H, D), 1 / math.sqrt(D)), randn((TC, H, D)), ch)
+        return c
+
+    out = {}
+    caches = [filled("bf16") for _ in range(2)]
+    whole = [filled("bf16", attn_workspace=False) for _ in range(2)]
+    for tq in (128, 1560):
+        q = randn((tq, H, D), 1 / math.sqrt(D))
+        o = torch.empty_like(q)
+        flop = 4.0 * H * tq * LK * D
+        ms = med(lambda i: caches[i % 2].attn(q, scale, out=o))
+        ms_whole = med(lambda i: whole[i % 2].attn(q, scale, out=o))
+        out[f"split_kv_tq{tq}"] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+                                   "ms_whole_items": ms_whole, "speedup": ms_whole / ms,
+                                   "what": f"bf16 attention, {tq} queries x 18720 keys x 12 heads; "
+                                           "items spread over all SMs vs whole items per CTA"}
+    del caches, whole
+    f4 = [filled("fp4", stage=True) for _ in range(2)]
+    hid = randn((LK, HD))
+    present = [0, 1, 2, 3]
+    ms = med(lambda i: f4[i % 2].recache(hid, wkv, gamma, present, GRID_H, GRID_W))
+    out["recache_fp4"] = {"ms": ms, "tflops": RECACHE_FLOP / (ms * 1e-3) / 1e12,
+                          "what": "recache of 18720 rows into an FP4 cache: the three projection "
+                                  "launches into the staging buffer, then the FP4 encode of the "
+                                  "four regions"}
+    hc = randn((TC, HD))
+    qo = torch.empty((TC, H, D), dtype=torch.bfloat16, device=dev)
+    ms = med(lambda i: f4[i % 2].project_append(hc, wqkv, None, gamma, W, GRID_H, GRID_W, q_out=qo))
+    out["project_append_fp4"] = {"ms": ms, "tflops": PROJECT_FLOP / (ms * 1e-3) / 1e12,
+                                 "what": "chunk [Q|K|V] projection with Q/K norm + RoPE, K/V "
+                                         "FP4-encoded into the ring slot (re-append of the "
+                                         "newest chunk)"}
+    for c in f4:
+        if c.last_device_error() != swl.KVC_OK:
+            raise RuntimeError("device error in the extra rows")
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Multi-rank bookkeeping (replicas: every rank runs the same step on its GPU)
 # ---------------------------------------------------------------------------
 def max_over_ranks(ms: float, dist, device) -> float:
@@ -291,6 +362,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rolling", action="store_true",
                     help="skip the 30-layer x 320-chunk rolling-stream leg")
+    ap.add_argument("--prewarm-s", type=float, default=0.3,
+                    help="seconds of pre-warm steps before the warm-up (0: none, e.g. for a "
+                         "profiler's launch list)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the rows timed outside the step (split-KV, FP4 recache/projection)")
     ap.add_argument("--layers", type=int, default=NLAYERS,
                     help="independent layer caches the steps rotate over (fewer: smaller "
                          "device footprint, e.g. for profiler captures)")
@@ -321,12 +397,14 @@ def main():
         return x.to(torch.bfloat16)
 
     wkv = randn((HD, 2 * HD), 0.02)
+    wqkv = randn((HD, 3 * HD), 0.02)
     gamma = torch.ones(HD, dtype=torch.float32, device=dev)
     layers = []
     nlayers = max(1, args.layers)
     for li in range(nlayers):
         L = {
-            "bf": swl.KVCache(H, D, TPF, CF, W, dtype="bf16", device=dev),
+            "bf": swl.KVCache(H, D, TPF, CF, W, dtype="bf16", device=dev,
+                              stage=2 * TC * HD * 4),  # the chunk projection's fp32 Q|K rows
             "f4": swl.KVCache(H, D, TPF, CF, W, dtype="fp4", device=dev),
             "q": randn((TC, H, D), 1 / math.sqrt(D)),
             "k": randn((TC, H, D), 1 / math.sqrt(D)),
@@ -334,6 +412,7 @@ def main():
             "k4": randn((TC, H, D), outliers=True),
             "v4": randn((TC, H, D), outliers=True),
             "hid": randn((LK, HD)),
+            "hc": randn((TC, HD)),  # hidden states of the new chunk
             "c": 0,
         }
         L["o"] = torch.empty_like(L["q"])
@@ -344,7 +423,8 @@ def main():
         L["c"] = W
         layers.append(L)
     scale = 1.0 / math.sqrt(D)
-    ROWS = ["recache", "evict_bf16", "append_bf16", "attn_bf16", "evict_fp4", "append_fp4", "attn_fp4"]
+    ROWS = ["recache", "evict_bf16", "project_append_bf16", "attn_bf16", "evict_fp4", "append_fp4",
+            "attn_fp4"]
 
     def step(L, evs=None, wkv_t=None):
         c = L["c"] + 1
@@ -353,7 +433,8 @@ def main():
         rec = (lambda: L["bf"].recache(L["hid"], w, gamma, present, GRID_H, GRID_W))
         ops = [rec,
                lambda: L["bf"].evict(c - W),
-               lambda: L["bf"].append(L["k"], L["v"], c),
+               lambda: L["bf"].project_append(L["hc"], wqkv, None, gamma, c, GRID_H, GRID_W,
+                                              q_out=L["q"]),
                lambda: L["bf"].attn(L["q"], scale, out=L["o"]),
                lambda: L["f4"].evict(c - W),
                lambda: L["f4"].append(L["k4"], L["v4"], c),
@@ -366,9 +447,10 @@ def main():
                 evs[i + 1].record()
         L["c"] = c
 
-    # recache (K GEMM, norm+RoPE, V GEMM), bf16 append copy, bf16 attention,
-    # FP4 append (amax, encode), FP4 attention; evict without scrub launches nothing
-    launches_per_step = 3 + 1 + 1 + 2 + 1
+    # recache (K GEMM, norm+RoPE, V GEMM), chunk projection (GEMM, norm+RoPE),
+    # bf16 attention, FP4 append (amax, encode), FP4 attention; evict without
+    # scrub launches nothing
+    launches_per_step = 3 + 2 + 1 + 2 + 1
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
           for _ in range(args.steps)]
@@ -380,7 +462,7 @@ def main():
     # state before the W warm-up steps.  A fresh process measured without it
     # showed host-side gaps (a launch-free evict taking 24 us instead of 2).
     prewarm, t_pw = 0, time.perf_counter()
-    while time.perf_counter() - t_pw < 0.3:
+    while time.perf_counter() - t_pw < args.prewarm_s:
         step(layers[prewarm % nlayers])
         prewarm += 1
         if prewarm % 8 == 0:
@@ -480,6 +562,7 @@ def main():
     e2e_value = job_tflops(ATTN_FLOP, world, e2e_ms)
 
     hbm = hbm_kernels(swl, dev, layers, randn)
+    extra = None if args.no_extra else extra_rows(swl, dev, randn, wkv, wqkv, gamma)
     for L in layers:
         for cache in (L["bf"], L["f4"]):
             st = cache.last_device_error()
@@ -500,8 +583,9 @@ def main():
         r["frac_hbm_peak"] = r["gbs"] / hbm_peak
     steps = args.steps
     per = {r: row_ms[r] / steps for r in ROWS}
-    flops = {"recache": RECACHE_FLOP, "attn_bf16": ATTN_FLOP, "attn_fp4": ATTN_FLOP}
-    bytes_ = {"append_bf16": APPEND_BF16_BYTES, "append_fp4": APPEND_FP4_BYTES,
+    flops = {"recache": RECACHE_FLOP, "attn_bf16": ATTN_FLOP, "attn_fp4": ATTN_FLOP,
+             "project_append_bf16": PROJECT_FLOP}
+    bytes_ = {"append_fp4": APPEND_FP4_BYTES,
               "attn_bf16": ATTN_BF16_BYTES, "attn_fp4": ATTN_FP4_BYTES, "recache": RECACHE_BYTES}
     rows = {}
     for r in ROWS:
@@ -533,8 +617,8 @@ def main():
                    "value": "bf16 chunk attention, 4680 queries x 18720 keys x 12 heads x 128 "
                             f"({ATTN_FLOP / 1e9:.2f} GFLOP per call), CUDA events around the call "
                             "inside each step, all ranks' calls over the slowest rank's time",
-                   "step": "recache + (evict, append, attention) on a bf16 cache + (evict, FP4 "
-                           "append, attention) on an FP4 cache",
+                   "step": "recache + (evict, [Q|K|V] projection appending K/V, attention) on a "
+                           "bf16 cache + (evict, FP4 append, attention) on an FP4 cache",
                    "step_gflop": STEP_FLOP / 1e9, "layers_rotated": nlayers,
                    "l2": f"inputs larger than L2: {nlayers} rotating layer caches, each step "
                          "touches > 200 MB (the L2 holds 126 MB)",
@@ -557,6 +641,7 @@ def main():
                         "attention through the public API, O device->host"},
         "rolling": rolling,
         "hbm_kernels": hbm,
+        "more_rows": extra,
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
