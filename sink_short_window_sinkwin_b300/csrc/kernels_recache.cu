@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
     recache_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
   using Smem = GemmSmem<BN>;
-  constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
+  // two accumulators of BN columns; TMEM is allocated in powers of two >= 32
+  constexpr uint32_t kCols = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -566,7 +567,7 @@ cudaError_t launch_project_chunk(const ProjectLaunch& r, cudaStream_t st) {
     case 512: return launch_project_t<256, 512>(r, st);
     case 768: return launch_project_t<256, 768>(r, st);
     case 1024: return launch_project_t<256, 1024>(r, st);
-    case 1536: return launch_project_t<256, 1536>(r, st);
+    case 1536: return launch_project_t<192, 1536>(r, st);  // 4608 = 24 x 192: whole waves at 4680 rows
     case 2048: return launch_project_t<256, 2048>(r, st);
     case 3072: return launch_project_t<256, 3072>(r, st);
     default: return cudaErrorInvalidValue;
