@@ -240,7 +240,8 @@ int32_t kvc_project_append(kvc_cache* c, const void* hidden, const void* w_qkv,
  * a tensor holding NaN or infinity are unspecified) as one tensor:
  *   amax = max|x|;  g = fl32(amax / 2688);   (g == 0: all codes and scales 0)
  *   per 16-block b: s = E4M3_rne_satfinite(fl32(fl32(amax_b / 6) / g));
- *   s == 0 or fl32(s*g) == 0: codes 0;  else t = fl32(|x| * fl32(1 / fl32(s*g))),
+ *   inv = fl32(1 / fl32(s*g));  s == 0, fl32(s*g) == 0 or inv infinite: scale
+ *   and codes 0 (only for amax below ~2^-115);  else t = fl32(|x| * inv),
  *   code = signbit(x) << 3 | E2M1_rne_satfinite(t).
  * codes: device uint8 [n/2] (element 2i in the low nibble); scales: device uint8
  * [n/16]; gscale: device float [1]; ws: device scratch of KVC_QUANT_WS_WORDS

@@ -15,8 +15,11 @@ none; the CUDA side follows the same order so codes match bit for bit):
   1. amax = max |x| over the tensor;  g = fl32(amax / 2688)   (2688 = 6 * 448)
      if g == 0 every scale and code is 0 and the stored g is 0.
   2. per block b of 16: s_f = fl32(fl32(amax_b / 6) / g);  s = E4M3_rne_satfinite(s_f)
-  3. if s == 0 or fl32(s*g) == 0: the block's codes are all 0x0
-     else inv = fl32(1 / fl32(s*g)); t = fl32(|x| * inv);
+  3. inv = fl32(1 / fl32(s*g)).  If s == 0, fl32(s*g) == 0 or inv overflows
+     to infinity (s*g below about 2^-128: only for tensors whose largest
+     magnitude is below about 2^-115), the block is stored as zeros: scale
+     byte 0 and codes 0x0 (a reading: the rule has no finite t there);
+     else t = fl32(|x| * inv);
           code = signbit(x) << 3 | E2M1_rne_satfinite(t)
   4. element 2i in the low nibble, 2i+1 in the high nibble of a byte.
 Decode: x_hat = e2m1(code) * s * g, exact in float64.
@@ -110,13 +113,15 @@ def quantize(x) -> tuple[np.ndarray, np.ndarray, np.float32]:
     s_code = e4m3_rne_satfinite(s_f)
     s_val = E4M3_POS[s_code].astype(np.float32)
     sg = s_val * g
-    dead = (s_code == 0) | (sg == np.float32(0.0))
-    with np.errstate(divide="ignore"):
-        inv = np.float32(1.0) / np.where(dead, np.float32(1.0), sg)
+    with np.errstate(divide="ignore", over="ignore"):
+        inv = np.float32(1.0) / np.where(sg == np.float32(0.0), np.float32(1.0), sg)
+    dead = (s_code == 0) | (sg == np.float32(0.0)) | ~np.isfinite(inv)
+    inv = np.where(dead, np.float32(1.0), inv).astype(np.float32)
     t = np.abs(blocks) * inv[:, None]
     mag = e2m1_rne_satfinite(t)
     code = (np.signbit(blocks).astype(np.uint8) << 3) | mag
     code[dead] = 0
+    s_code = np.where(dead, np.uint8(0), s_code).astype(np.uint8)
     packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
     return (packed.reshape(lead + (D // 2,)), s_code.reshape(lead + (D // 16,)), g)
 

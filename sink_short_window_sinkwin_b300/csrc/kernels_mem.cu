@@ -147,7 +147,9 @@ struct ScaleTab {
 __device__ __forceinline__ void build_scale_tab(ScaleTab& t, float g, int tid, int nthreads) {
   for (int s = tid; s < 128; s += nthreads) {
     const float sg = __fmul_rn(e4m3_value((uint32_t)s), g);
-    t.e[s] = make_float2(sg, sg != 0.0f ? __frcp_rn(sg) : 0.0f);
+    const float r = sg != 0.0f ? __frcp_rn(sg) : 0.0f;
+    // no finite reciprocal (s * g below ~2^-128): the block is stored as zeros
+    t.e[s] = r < 3.0e38f ? make_float2(sg, r) : make_float2(0.0f, 0.0f);
   }
 }
 
@@ -193,17 +195,38 @@ __device__ __forceinline__ uint32_t block_amax_bits(const uint32_t (&w)[8]) {
   return max(m & 0xFFFFu, m >> 16);
 }
 
+// E4M3 code of fl32(a / g) (a >= 0 finite, g > 0), round to nearest even,
+// saturating -- without a division on the common path.  q = fl32(a * ginv)
+// (ginv = fl32(1 / g)) corrected by one FMA residual step is within an ulp or
+// two of the correctly rounded quotient, so whenever the E4M3 rounding of
+// q - 2 ulp and of q + 2 ulp agree (every case but quotients within a few ulps
+// of a rounding midpoint between two E4M3 values), that code is the code of
+// the correctly rounded quotient as well; otherwise the quotient is computed
+// exactly.
+__device__ __forceinline__ uint32_t e4m3_scale_code(float a, float g, float ginv) {
+  if (!(ginv < 3.0e38f)) return e4m3_rne_satfinite(__fdiv_rn(a, g));  // g below 2^-127
+  const float q0 = __fmul_rn(a, ginv);
+  const float q = __fmaf_rn(__fmaf_rn(-q0, g, a), ginv, q0);
+  const uint32_t qb = __float_as_uint(q);
+  const float lo = qb >= 2u ? __uint_as_float(qb - 2u) : 0.0f;
+  const float hi = __uint_as_float(qb + 2u);  // q < 2^127: no overflow into inf
+  uint16_t pair;  // E4M3 codes of hi (high byte) and lo (low byte)
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+  if ((pair >> 8) == (pair & 0xFFu)) return pair & 0xFFu;
+  return e4m3_rne_satfinite(__fdiv_rn(a, g));  // near a rounding midpoint
+}
+
 // One 16-element block (8 words of bf16 pairs, block amax given as bf16
 // magnitude bits) under tensor scale g: its E4M3 scale byte and 8 bytes of
 // packed E2M1 codes, in the fixed fp32 order of the encode rule.
 __device__ __forceinline__ void encode_block_amax(const uint32_t (&w)[8], uint32_t amax_bits, float g,
-                                                  const ScaleTab& tab, uint32_t& s, uint32_t& lo,
-                                                  uint32_t& hi) {
+                                                  float ginv, const ScaleTab& tab, uint32_t& s,
+                                                  uint32_t& lo, uint32_t& hi) {
   s = 0;
   lo = 0;
   hi = 0;
   if (g == 0.0f) return;
-  s = e4m3_rne_satfinite(__fdiv_rn(div6_bf16(__uint_as_float(amax_bits << 16)), g));
+  s = e4m3_scale_code(div6_bf16(__uint_as_float(amax_bits << 16)), g, ginv);
   const float2 sgi = tab.e[s];  // {s * g, 1 / (s * g)}
   if (s == 0 || sgi.x == 0.0f) {
     s = 0;
@@ -222,9 +245,9 @@ __device__ __forceinline__ void encode_block_amax(const uint32_t (&w)[8], uint32
   }
 }
 
-__device__ __forceinline__ void encode_block(const uint32_t (&w)[8], float g, const ScaleTab& tab,
-                                             uint32_t& s, uint32_t& lo, uint32_t& hi) {
-  encode_block_amax(w, block_amax_bits(w), g, tab, s, lo, hi);
+__device__ __forceinline__ void encode_block(const uint32_t (&w)[8], float g, float ginv,
+                                             const ScaleTab& tab, uint32_t& s, uint32_t& lo, uint32_t& hi) {
+  encode_block_amax(w, block_amax_bits(w), g, ginv, tab, s, lo, hi);
 }
 
 // ---------------------------------------------------------------------------
@@ -286,8 +309,8 @@ __device__ __forceinline__ void load_pair(const uint4* x, int i, int cnt, BlockP
     }
   }
 }
-__device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, float g, const ScaleTab& tab,
-                                            uint2* codes, uint8_t* scales) {
+__device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, float g, float ginv,
+                                            const ScaleTab& tab, uint2* codes, uint8_t* scales) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int b = i + h * kEncThreads;
@@ -295,7 +318,7 @@ __device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, 
       const uint32_t w[8] = {r.v[2 * h].x,     r.v[2 * h].y,     r.v[2 * h].z,     r.v[2 * h].w,
                              r.v[2 * h + 1].x, r.v[2 * h + 1].y, r.v[2 * h + 1].z, r.v[2 * h + 1].w};
       uint32_t sc, lo, hi;
-      encode_block(w, g, tab, sc, lo, hi);
+      encode_block(w, g, ginv, tab, sc, lo, hi);
       codes[b] = make_uint2(lo, hi);
       scales[b] = (uint8_t)sc;
     }
@@ -330,16 +353,17 @@ __global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, i
   }
   __syncthreads();
   const float g = gsh;
+  const float ginv = g != 0.0f ? __frcp_rn(g) : 0.0f;
   if (blockIdx.x == 0 && tid == 0) *job.gscale = g;
   build_scale_tab(tab, g, tid, kEncThreads);
   __syncthreads();
   while (i < cnt) {
     load_pair(x, i + 2 * kEncThreads, cnt, B);
-    encode_pair(A, i, cnt, g, tab, codes, scales);
+    encode_pair(A, i, cnt, g, ginv, tab, codes, scales);
     i += 2 * kEncThreads;
     if (i >= cnt) break;
     load_pair(x, i + 2 * kEncThreads, cnt, A);
-    encode_pair(B, i, cnt, g, tab, codes, scales);
+    encode_pair(B, i, cnt, g, ginv, tab, codes, scales);
     i += 2 * kEncThreads;
   }
 }

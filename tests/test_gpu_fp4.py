@@ -69,6 +69,46 @@ def test_quant_bitexact_edge_values(swl):
     _check_quant(swl, y, "ragged size")
 
 
+def _near_midpoint_maxima(amax_t: float, n_ulp: int = 8):
+    """bf16 block maxima b <= amax_t whose scale quotient fl32(fl32(b/6)/g),
+    g = fl32(amax_t/2688), lies within n_ulp float32 ulps of a rounding midpoint
+    between two E4M3 values (so a quotient off by an ulp could round to the
+    other code)."""
+    f32 = np.float32
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)  # positive finite bf16
+    b = (bits << 16).view(np.float32)
+    b = b[b <= f32(amax_t)]
+    g = f32(f32(amax_t) / ofp4.G_DIVISOR)
+    q = (b / f32(6.0)).astype(f32) / g
+    qb = q.view(np.uint32)
+    lo = np.maximum(qb.astype(np.int64) - n_ulp, 0).astype(np.uint32).view(np.float32)
+    hi = (qb + n_ulp).view(np.float32)
+    near = ofp4.e4m3_rne_satfinite(lo) != ofp4.e4m3_rne_satfinite(hi)
+    return b[near]
+
+
+def test_quant_bitexact_near_scale_midpoints(swl):
+    """Blocks whose scale quotient sits within a few ulps of an E4M3 rounding
+    midpoint, for tensor maxima over many magnitudes: the encoder's fast
+    scale path must defer to the exact quotient there, codes and scales
+    bit-exact against the oracle."""
+    rng = np.random.default_rng(9)
+    for amax_t in (1.0, 3.734375, 1.0e-3, 8.5e5, 2.0 ** -100, 2.0 ** -120, 448.0 * 6.0, 0.15625):
+        amax_t = float(torch.tensor(amax_t).to(torch.bfloat16).float())
+        maxima = _near_midpoint_maxima(amax_t)
+        # g = amax_t / 2688 is a normal float except for the smallest tensor,
+        # where 1/g overflows and every block takes the exact quotient
+        assert len(maxima) > 0 or amax_t < 2.0 ** -115, amax_t
+        spread = amax_t * np.exp2(-rng.uniform(0, 40, 64))
+        maxima = np.concatenate([maxima, spread.astype(np.float32)])
+        blocks = np.zeros((len(maxima) + 1, 16), np.float32)
+        blocks[:-1, 0] = maxima
+        blocks[:-1, 1:] = maxima[:, None] * rng.uniform(-1, 1, (len(maxima), 15)).astype(np.float32)
+        blocks[-1, 0] = amax_t  # the tensor maximum
+        x = torch.from_numpy(blocks.reshape(-1)).to(torch.bfloat16)
+        _check_quant(swl, x, f"near-midpoint blocks, tensor amax {amax_t:g} ({len(maxima)} blocks)")
+
+
 def _fp4_stream(swl, sh, cfg, steps, dist):
     cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
                         sh.window_chunks, dtype="fp4")

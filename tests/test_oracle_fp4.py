@@ -171,3 +171,30 @@ def test_reconstruction_error_bound():
     assert np.all(np.abs(x) / sv <= 6.0 * (1 + 2 ** -3) + 1e-6)
     rel = np.linalg.norm(xh - x) / np.linalg.norm(x)
     assert rel < 0.12
+
+
+def test_tiny_tensor_blocks_without_finite_reciprocal():
+    """A tensor whose largest magnitude is 2^-120: g = 2^-120 / 2688 is an fp32
+    subnormal, and blocks whose s*g has no finite fp32 reciprocal are stored
+    as zeros.  Every block still decodes within the error bound (a zero
+    element never decodes to a nonzero value), and the zeroed blocks are only
+    blocks whose values are all below 2^-124."""
+    rng = np.random.default_rng(5)
+    amax = np.float32(2.0 ** -120)
+    mags = amax * np.exp2(-rng.uniform(0, 14, (256, 1))).astype(np.float32)
+    x = (mags * rng.uniform(-1, 1, (256, 16))).astype(np.float32)
+    x[rng.random(x.shape) < 0.2] = 0.0
+    x[0, 0] = amax
+    p, s, g = fp4.quantize(x)
+    assert 0 < g < np.finfo(np.float32).tiny
+    xh = fp4.dequantize(p, s, g)
+    c = fp4.unpack_codes(p)
+    zeroed = s[:, 0] == 0
+    assert zeroed.any() and (~zeroed).any()
+    assert not c[zeroed].any()
+    assert np.all(np.abs(x[zeroed]) < 2.0 ** -124)
+    sv = fp4.E4M3_ALL[s[:, 0]] * float(g)
+    live = ~zeroed
+    err = np.abs(xh - x.astype(np.float64))
+    assert np.all(err[live] <= sv[live][:, None] * 1.0)
+    assert np.all(xh[x == 0] == 0)
