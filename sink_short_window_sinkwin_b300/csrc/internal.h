@@ -127,5 +127,8 @@ bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
                          uint32_t box1, uint32_t box2, bool swizzle128);
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                          uint64_t stride1_bytes, uint32_t box0, uint32_t box1, bool swizzle128);
+// the same with a swizzle of 0, 32, 64 or 128 bytes
+bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                            uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes);
 
 }  // namespace kvc

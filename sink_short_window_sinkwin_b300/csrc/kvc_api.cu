@@ -50,6 +50,19 @@ bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
 
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                          uint64_t stride1_bytes, uint32_t box0, uint32_t box1, bool swizzle128) {
+  return encode_tmap_2d_bf16_sw(m, base, d0, d1, stride1_bytes, box0, box1, swizzle128 ? 128 : 0);
+}
+
+bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                            uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes) {
+  CUtensorMapSwizzle sw;
+  switch (swizzle_bytes) {
+    case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return false;
+  }
   auto fn = get_encode();
   if (!fn) return false;
   cuuint64_t dims[2] = {d0, d1};
@@ -57,8 +70,7 @@ bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

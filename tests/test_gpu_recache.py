@@ -82,15 +82,43 @@ def test_recache_tiny_then_attention(swl):
 
 
 def test_recache_two_column_tiles_noncontiguous_positions(swl):
-    """H*D = 512: the K row spans two 256-wide GEMM tiles, so the RMSNorm needs
-    the whole parked fp32 row; 180-token chunks make row tiles straddle chunks,
-    and chunks {0, 97, 98, 99} put frame positions far apart (294..299 next to
-    0..2)."""
+    """H*D = 512: one CTA holds the whole K row (fused launch, a cluster of
+    one); 180-token chunks make row tiles straddle chunks, and chunks
+    {0, 97, 98, 99} put frame positions far apart (294..299 next to 0..2)."""
     sh = Shapes(4, 128, 60, 3, 3, 6, 10)
     cache, model = _fill(swl, sh, 99)
     assert model.present_chunks() == [0, 97, 98, 99]
     _recache_both(swl, sh, cache, model, 44)
     _compare_cache(cache, model, sh, what="two tiles")
+
+
+@pytest.mark.parametrize("heads,head_dim", [(8, 128), (8, 64), (16, 32), (16, 128)])
+def test_recache_fused_cluster_widths(swl, heads, head_dim):
+    """The fused launch at H*D = 1024, 512, 512 and 2048: clusters of 2, 1, 1
+    and 4 CTAs exchange per-row partial sums of squares; head widths 128, 64
+    and 32 change how the 32-column chunks map to rotation pairs and heads.
+    Four 120-token chunks (480 rows) end the last row tile inside the tile,
+    and chunks {0, 4, 5, 6} make the frame positions jump."""
+    sh = Shapes(heads, head_dim, 40, 3, 3, 4, 10)
+    cache, model = _fill(swl, sh, 6)
+    assert model.present_chunks() == [0, 4, 5, 6]
+    _recache_both(swl, sh, cache, model, 17, gamma_rand=True)
+    _compare_cache(cache, model, sh, what=f"fused H*D={heads * head_dim} D={head_dim}")
+
+
+@pytest.mark.parametrize("shape", [(8, 128, 64, 2, 3, 2, 32), (4, 128, 200, 1, 3, 2, 100),
+                                   (4, 128, 60, 3, 3, 6, 10)])
+def test_recache_fused_rotation_paths(swl, shape):
+    """The fused launch's rotation and store paths: a 2 x 32 grid (every warp's
+    32 rows share one grid row and at most two frames: per-warp frame/row
+    tables, column table, 8-row bulk stores); a 2 x 100 grid (the column table
+    would exceed its space: per-row column rotations); 180-token chunks (not a
+    multiple of 8 rows: lane stores) with a 6 x 10 grid (up to four grid rows
+    per warp: per-row frame/row rotations)."""
+    sh = Shapes(*shape)
+    cache, model = _fill(swl, sh, 5)
+    _recache_both(swl, sh, cache, model, 23, gamma_rand=True)
+    _compare_cache(cache, model, sh, what=f"fused rotation paths {shape}")
 
 
 @pytest.mark.parametrize("heads,head_dim", [(1, 128), (2, 128), (6, 128)])
