@@ -60,10 +60,9 @@ TRAFFIC = {
     # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
     "sinkwin_attn_kernel<128,false>": {"bytes": 305278720 + 26565120, "src_sha": "b4ae518685bd2dfc"},
     "sinkwin_attn_kernel<128,true>": {"bytes": 47181056 + 4062208, "src_sha": "b4ae518685bd2dfc"},
-    # K GEMM + norm + V GEMM of one recache; profiles/recache_gemm_layer1p3b.md
-    "recache_gemm_kernel<256,*> x2 + recache_norm_rope_kernel": {
-        "bytes": (62334208 + 60034048) + (115096064 + 15608320) + (62250752 + 19588608),
-        "src_sha": "c2165c20461392cd"},
+    # the fused K/V recache launch (one launch each, two launches captured);
+    # summary in profiles/recache_gemm_layer1p3b.md
+    "recache_fused_kernel": {"bytes": 67167488 + 70382592, "src_sha": "9b989b46f5922b6e"},
 }
 
 
@@ -316,8 +315,8 @@ def extra_rows(swl, dev, randn, wkv, wqkv, gamma, runs: int = 12):
     present = [0, 1, 2, 3]
     ms = med(lambda i: f4[i % 2].recache(hid, wkv, gamma, present, GRID_H, GRID_W))
     out["recache_fp4"] = {"ms": ms, "tflops": RECACHE_FLOP / (ms * 1e-3) / 1e12,
-                          "what": "recache of 18720 rows into an FP4 cache: the three projection "
-                                  "launches into the staging buffer, then the FP4 encode of the "
+                          "what": "recache of 18720 rows into an FP4 cache: the fused projection "
+                                  "launch into the staging buffer, then the FP4 encode of the "
                                   "four regions"}
     hc = randn((TC, HD))
     qo = torch.empty((TC, H, D), dtype=torch.bfloat16, device=dev)
@@ -447,10 +446,10 @@ def main():
                 evs[i + 1].record()
         L["c"] = c
 
-    # recache (K GEMM, norm+RoPE, V GEMM), chunk projection (GEMM, norm+RoPE),
+    # recache (one fused K/V launch), chunk projection (GEMM, norm+RoPE),
     # bf16 attention, FP4 append (amax, encode), FP4 attention; evict without
     # scrub launches nothing
-    launches_per_step = 3 + 2 + 1 + 2 + 1
+    launches_per_step = 1 + 2 + 1 + 2 + 1
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
           for _ in range(args.steps)]
@@ -603,7 +602,7 @@ def main():
         rows[r] = d
     dom = max(("attn_bf16", "attn_fp4", "recache"), key=lambda r: per[r])
     kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>", "attn_fp4": "sinkwin_attn_kernel<128,true>",
-             "recache": "recache_gemm_kernel<256,*> x2 + recache_norm_rope_kernel"}[dom]
+             "recache": "recache_fused_kernel"}[dom]
     src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_attn.cu",
            "recache": "kernels_recache.cu"}[dom]
     tr = TRAFFIC.get(kname)

@@ -92,11 +92,12 @@ def test_recache_two_column_tiles_noncontiguous_positions(swl):
     _compare_cache(cache, model, sh, what="two tiles")
 
 
-@pytest.mark.parametrize("heads,head_dim", [(8, 128), (8, 64), (16, 32), (16, 128)])
+@pytest.mark.parametrize("heads,head_dim", [(8, 128), (8, 64), (16, 64), (16, 128), (16, 32)])
 def test_recache_fused_cluster_widths(swl, heads, head_dim):
-    """The fused launch at H*D = 1024, 512, 512 and 2048: clusters of 2, 1, 1
-    and 4 CTAs exchange per-row partial sums of squares; head widths 128, 64
-    and 32 change how the 32-column chunks map to rotation pairs and heads.
+    """The fused launch at H*D = 1024, 512, 1024 and 2048: clusters of 2, 1, 2
+    and 4 CTAs exchange per-row partial sums of squares; head widths 128 and
+    64 change how the 32-column chunks map to rotation pairs and heads.  Head
+    width 32 (H*D = 512) takes the three-launch path.
     Four 120-token chunks (480 rows) end the last row tile inside the tile,
     and chunks {0, 4, 5, 6} make the frame positions jump."""
     sh = Shapes(heads, head_dim, 40, 3, 3, 4, 10)
