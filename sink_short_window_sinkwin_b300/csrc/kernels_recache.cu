@@ -432,7 +432,12 @@ constexpr int kTwMax = 1536;      // grid_w x column band pairs held in the colu
 
 struct FusedParams {
   int32_t rows, HD, Tc, D, tpf, grid_w, pf, ph;
-  int32_t nitems;  // 2 x row tiles
+  // Work items.  Cluster launch (vonly == 0): K and V of row tiles
+  // [0, rt_split) alternate (item 2 t is K, 2 t + 1 is V of row tile t), then
+  // K alone of row tiles [rt_split, row tiles).  Cluster-free launch
+  // (vonly == 1, on the SMs no cluster fits): V of row tiles [rt_split, row
+  // tiles), one 512-column block per item.
+  int32_t nitems, rt_split, vonly;
   float eps;
   int32_t region[kMaxSeg];
   int64_t frame0[kMaxSeg];
@@ -459,6 +464,20 @@ struct __align__(1024) FusedSmem {
   uint32_t tmem_base;
   int32_t abort_flag;
 };
+
+struct FItem {
+  int m0;      // first row of the tile
+  bool is_k;   // K (normed, rotated) or V
+  int cb;      // 512-column block of the projection this CTA computes
+};
+__device__ __forceinline__ FItem fused_item(const FusedParams& p, int it, int rank) {
+  if (p.vonly) {
+    const int ncb = p.HD / FW;
+    return FItem{(p.rt_split + it / ncb) * RM, false, it % ncb};
+  }
+  if (it < 2 * p.rt_split) return FItem{(it >> 1) * RM, (it & 1) == 0, rank};
+  return FItem{(p.rt_split + (it - 2 * p.rt_split)) * RM, true, rank};
+}
 
 // Slot of 16-byte piece c (0..3) of bf16 staging row r (16 words a row).  Writes
 // (8 lanes = 8 consecutive rows, one piece each) and transposed reads (8 lanes =
@@ -598,8 +617,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         int na = 0, nb = 0;  // A and B ring positions
         bool ok = true;
         for (int it = cl; it < p.nitems && ok; it += ncl) {
-          const int m0 = (it >> 1) * RM;
-          const int c0 = (it & 1) * p.HD + rank * FW;  // first weight column of this CTA
+          const FItem fi = fused_item(p, it, rank);
+          const int m0 = fi.m0;
+          const int c0 = (fi.is_k ? 0 : p.HD) + fi.cb * FW;  // first weight column of this CTA
           for (int kb = 0; kb < nk && ok; ++kb) {
             {
               const int s = na % kFASlots, u = na / kFASlots;
@@ -692,11 +712,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int nfh = p.pf + p.ph;       // pairs of the frame and row bands
     const int nw = p.D / 2 - nfh;      // pairs of the column band
     const int64_t ld = p.HD / 8;       // output row stride in 16-byte pieces
-    const int gcol0 = rank * FW + half * 256;
     int j = 0, nkit = 0;
     for (int it = cl; it < p.nitems; it += ncl, ++j) {
-      const bool is_k = (it & 1) == 0;
-      const int m0 = (it >> 1) * RM;
+      const FItem fi = fused_item(p, it, rank);
+      const bool is_k = fi.is_k;
+      const int m0 = fi.m0;
+      const int gcol0 = fi.cb * FW + half * 256;
       const int gr = m0 + rloc;
       const int row0 = m0 + q * 32;
       int64_t my_dest = 0, fr = 0;
@@ -953,6 +974,38 @@ int fused_max_clusters(int ncta, size_t smem) {
   return n;
 }
 
+// A second stream and two events per host thread and device, created on first
+// use and kept (host objects only; no device memory): the fused recache's
+// cluster-free launch runs on it, forked from and joined back to the caller's
+// stream with the events (this also holds under stream capture).
+cudaError_t side_stream(cudaStream_t* s, cudaEvent_t* fork, cudaEvent_t* join) {
+  struct Side {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+  };
+  thread_local Side sides[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  Side& d = sides[dev];
+  if (!d.s) {
+    Side n;
+    cudaError_t e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (n.join) cudaEventDestroy(n.join);
+      if (n.fork) cudaEventDestroy(n.fork);
+      if (n.s) cudaStreamDestroy(n.s);
+      return e;
+    }
+    d = n;
+  }
+  *s = d.s;
+  *fork = d.fork;
+  *join = d.join;
+  return cudaSuccess;
+}
+
 // H*D a multiple of 512 (at most 4 x 512) and D in {64, 128}: one
 // fused launch (K and V items, the norm in the K epilogue).
 bool recache_fusable(int H, int D) {
@@ -985,7 +1038,6 @@ cudaError_t launch_recache_fused(const RecacheLaunch& r, cudaStream_t st) {
   p.k = static_cast<__nv_bfloat16*>(r.k);
   p.v = static_cast<__nv_bfloat16*>(r.v);
   p.dev_err = r.dev_err;
-  p.nitems = 2 * ((r.rows + RM - 1) / RM);
   p.w_tab = r.grid_w * (r.D / 2 - p.pf - p.ph) <= kTwMax;
   // bulk stores of 8-row boxes: every 8-row group of a tile lies in one chunk
   p.tma_out = r.Tc % 8 == 0;
@@ -1019,12 +1071,45 @@ cudaError_t launch_recache_fused(const RecacheLaunch& r, cudaStream_t st) {
     }
     if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
   }
-  const int ncta = HD / FW;
-  int ncl = fused_max_clusters(ncta, smem);
+  const int ncta = HD / FW, nrt = (r.rows + RM - 1) / RM;
+  const int ncl = fused_max_clusters(ncta, smem);
   if (ncl <= 0) return cudaErrorInvalidConfiguration;
-  if (ncl > p.nitems) ncl = p.nitems;
+  // SMs that no cluster fits on (13 of 148 for 3-CTA clusters) take the V
+  // items of the last x row tiles in a second, cluster-free launch beside the
+  // first: x balances the two by the measured item costs (a K item, with its
+  // norm and rotation epilogue, takes about 1.43 times a V item)
+  const int nsm = attn_sm_count();
+  const int nfree = nsm - ncl * ncta;
+  int x = 0;
+  if (nfree > 0) {
+    constexpr double kCostK = 1.43, kCostV = 1.0;
+    double best = (nrt * kCostK + nrt * kCostV) / ncl;
+    for (int xx = 1; xx <= nrt; ++xx) {
+      const double ta = (nrt * kCostK + (nrt - xx) * kCostV) / ncl;
+      const double tb = (double)((xx * ncta + nfree - 1) / nfree) * kCostV;
+      const double t = ta > tb ? ta : tb;
+      if (t < best - 1e-9) {
+        best = t;
+        x = xx;
+      }
+    }
+  }
+  p.vonly = 0;
+  p.rt_split = nrt - x;
+  p.nitems = nrt + p.rt_split;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  if (x > 0) {
+    // the side launch starts with the main one: both wait for the work already
+    // in `st`, and `st` waits for the side launch before anything after it
+    e = side_stream(&side, &ev_fork, &ev_join);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(ev_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev_fork, 0);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(ncta * ncl), 1, 1);
+  cfg.gridDim = dim3((unsigned)(ncta * (ncl < p.nitems ? ncl : p.nitems)), 1, 1);
   cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1035,7 +1120,19 @@ cudaError_t launch_recache_fused(const RecacheLaunch& r, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recache_fused_kernel, ta, tb, tk, tv, tk32, tv32, p);
+  e = cudaLaunchKernelEx(&cfg, recache_fused_kernel, ta, tb, tk, tv, tk32, tv32, p);
+  if (e != cudaSuccess || x == 0) return e;
+  FusedParams pv = p;
+  pv.vonly = 1;
+  pv.nitems = x * ncta;
+  cfg.gridDim = dim3((unsigned)(nfree < pv.nitems ? nfree : pv.nitems), 1, 1);
+  cfg.stream = side;
+  attr[0].val.clusterDim.x = 1;
+  e = cudaLaunchKernelEx(&cfg, recache_fused_kernel, ta, tb, tk, tv, tk32, tv32, pv);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev_join, side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_join, 0);
+  return e;
 }
 
 template <int HD>
