@@ -60,9 +60,9 @@ TRAFFIC = {
     # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
     "sinkwin_attn_kernel<128,false>": {"bytes": 305278720 + 26565120, "src_sha": "b4ae518685bd2dfc"},
     "sinkwin_attn_kernel<128,true>": {"bytes": 47181056 + 4062208, "src_sha": "b4ae518685bd2dfc"},
-    # the fused K/V recache launch (one launch each, two launches captured);
-    # summary in profiles/recache_gemm_layer1p3b.md
-    "recache_fused_kernel": {"bytes": 67167488 + 70382592, "src_sha": "9b989b46f5922b6e"},
+    # the fused recache: the cluster launch and the cluster-free launch beside
+    # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
+    "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "0c244feec41d7cfd"},
 }
 
 
