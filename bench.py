@@ -446,10 +446,10 @@ def main():
                 evs[i + 1].record()
         L["c"] = c
 
-    # recache (one fused K/V launch), chunk projection (GEMM, norm+RoPE),
-    # bf16 attention, FP4 append (amax, encode), FP4 attention; evict without
-    # scrub launches nothing
-    launches_per_step = 1 + 2 + 1 + 2 + 1
+    # recache (the fused cluster launch and its cluster-free side launch),
+    # chunk projection (GEMM, norm+RoPE), bf16 attention, FP4 append (amax,
+    # encode), FP4 attention; evict without scrub launches nothing
+    launches_per_step = 2 + 2 + 1 + 2 + 1
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
           for _ in range(args.steps)]
