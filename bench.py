@@ -316,8 +316,8 @@ def extra_rows(swl, dev, randn, wkv, wqkv, gamma, runs: int = 12):
     ms = med(lambda i: f4[i % 2].recache(hid, wkv, gamma, present, GRID_H, GRID_W))
     out["recache_fp4"] = {"ms": ms, "tflops": RECACHE_FLOP / (ms * 1e-3) / 1e12,
                           "what": "recache of 18720 rows into an FP4 cache: the fused projection "
-                                  "launch into the staging buffer, then the FP4 encode of the "
-                                  "four regions"}
+                                  "launches into the staging buffer, then one FP4 encode of the "
+                                  "four regions' K and V (8 tensors, two launches)"}
     hc = randn((TC, HD))
     qo = torch.empty((TC, H, D), dtype=torch.bfloat16, device=dev)
     ms = med(lambda i: f4[i % 2].project_append(hc, wqkv, None, gamma, W, GRID_H, GRID_W, q_out=qo))

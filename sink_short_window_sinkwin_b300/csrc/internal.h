@@ -27,9 +27,11 @@ cudaError_t launch_copy2(void* dst0, const void* src0, void* dst1, const void* s
 cudaError_t launch_fill(void* const* dst, const size_t* bytes, const uint32_t* words, int n,
                         cudaStream_t st);
 
-// FP4 encode of up to two tensors (x1 may be null), n elements each, n % 16 == 0.
-// ws: 2 * kQuantPartials int32 words (per-CTA partial maxima).
-constexpr int kQuantPartials = 256;
+// FP4 encode of up to kMaxQuantJobs tensors of n elements each (n % 16 == 0),
+// each its own tensor.  ws: ws_words int32 words of scratch (per-CTA partial
+// maxima, ws_words / njobs per tensor, at least one).
+constexpr int kQuantPartials = 256;  // partial maxima of one tensor, at most
+constexpr int kMaxQuantJobs = 2 * kMaxSeg;
 struct QuantJob {
   const void* x;
   uint8_t* codes;
@@ -38,7 +40,7 @@ struct QuantJob {
 };
 // Two launches: per-CTA partial maxima, then the block encode as a programmatic
 // dependent launch (its first loads overlap the end of the first pass).
-cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
+cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws, int ws_words,
                              cudaStream_t st);
 
 // ---- attention (kernels_attn.cu) ----

@@ -102,7 +102,7 @@ int mem_grid(size_t n16, int ny) {
 // FP4 encode
 // ---------------------------------------------------------------------------
 struct QuantJobs {
-  QuantJob j[2];
+  QuantJob j[kMaxQuantJobs];
 };
 
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
@@ -260,17 +260,18 @@ __device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint4 v) {
 }
 
 // Pass 1: CTA (x, j) takes a contiguous range of tensor j's 16-byte vectors and
-// writes the range's magnitude maximum (bf16 bits) to ws[j * kQuantPartials + x]
+// writes the range's magnitude maximum (bf16 bits) to ws[j * stride + x]
 // (no atomics, nothing to zero).  Two CTAs per SM, six loads in flight per
 // thread on every trip.
 constexpr int kAmaxThreads = 1024;
 constexpr int kAmaxUnroll = 6;
-__global__ void __launch_bounds__(kAmaxThreads, 2) amax_kernel(QuantJobs jobs, int64_t n,
-                                                               int32_t* __restrict__ ws) {
+__global__ void __launch_bounds__(kAmaxThreads, 2) amax_kernel(const __grid_constant__ QuantJobs jobs,
+                                                               int64_t n, int32_t* __restrict__ ws,
+                                                               int stride) {
   pdl_launch_dependents();  // the encode pass may take the SM slots this grid frees
   __shared__ uint32_t red[32];
-  // select, not index: a dynamic index would copy the parameter struct to local memory
-  const uint4* x = reinterpret_cast<const uint4*>(blockIdx.y ? jobs.j[1].x : jobs.j[0].x);
+  // (a __grid_constant__ parameter is indexed in place, not copied)
+  const uint4* x = reinterpret_cast<const uint4*>(jobs.j[blockIdx.y].x);
   const int64_t n8 = n >> 3, G = gridDim.x;
   const int64_t v1 = ((int64_t)blockIdx.x + 1) * n8 / G;
   uint32_t acc = 0;
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kAmaxThreads, 2) amax_kernel(QuantJobs jobs, i
   }
   acc &= 0x7FFF7FFFu;
   const uint32_t m = block_max_u32(max(acc & 0xFFFFu, acc >> 16), red);
-  if (threadIdx.x == 0) ws[blockIdx.y * kQuantPartials + blockIdx.x] = (int32_t)m;
+  if (threadIdx.x == 0) ws[blockIdx.y * stride + blockIdx.x] = (int32_t)m;
 }
 
 // Pass 2: CTA (x, j) encodes a contiguous range of tensor j's 16-element
@@ -324,12 +325,12 @@ __device__ __forceinline__ void encode_pair(const BlockPair& r, int i, int cnt, 
     }
   }
 }
-__global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, int64_t n,
-                                                               const int32_t* __restrict__ ws,
-                                                               int parts) {
+__global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(const __grid_constant__ QuantJobs jobs,
+                                                               int64_t n, const int32_t* __restrict__ ws,
+                                                               int stride, int parts) {
   __shared__ float gsh;
   __shared__ ScaleTab tab;
-  const QuantJob job = blockIdx.y ? jobs.j[1] : jobs.j[0];
+  const QuantJob& job = jobs.j[blockIdx.y];
   const int tid = threadIdx.x;
   const int64_t nb = n >> 4, G = gridDim.x;
   const int64_t b0 = (int64_t)blockIdx.x * nb / G;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) quant_kernel(QuantJobs jobs, i
 #pragma unroll
     for (int u = 0; u < kQuantPartials / 32; ++u) {
       const int k = tid + 32 * u;
-      if (k < parts) m = max(m, (uint32_t)__ldcg(ws + blockIdx.y * kQuantPartials + k));
+      if (k < parts) m = max(m, (uint32_t)__ldcg(ws + blockIdx.y * stride + k));
     }
     m = __reduce_max_sync(0xffffffffu, m);
     if (tid == 0) gsh = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
@@ -411,19 +412,23 @@ cudaError_t launch_fill(void* const* dst, const size_t* bytes, const uint32_t* w
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws,
+cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t* ws, int ws_words,
                              cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+  if (njobs < 1 || njobs > kMaxQuantJobs) return cudaErrorInvalidValue;
+  const int stride = ws_words / njobs;  // partial-maximum words per tensor
+  if (stride < 1) return cudaErrorInvalidValue;
   QuantJobs qj{};
   for (int i = 0; i < njobs; ++i) qj.j[i] = jobs[i];
   const int nsm = attn_sm_count();
   // pass 1: two 1024-thread CTAs per SM over all tensors
-  int parts = 2 * nsm / njobs;
+  int64_t parts = 2 * (int64_t)nsm / njobs;
   if (parts > kQuantPartials) parts = kQuantPartials;
+  if (parts > stride) parts = stride;
   const int64_t n8 = n >> 3;
-  if (parts > n8) parts = (int)n8;
-  amax_kernel<<<dim3(parts, njobs), kAmaxThreads, 0, st>>>(qj, n, ws);
+  if (parts > n8) parts = n8;
+  if (parts < 1) parts = 1;
+  amax_kernel<<<dim3((unsigned)parts, njobs), kAmaxThreads, 0, st>>>(qj, n, ws, stride);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // pass 2: two 512-thread CTAs per SM over all tensors, as a dependent launch
@@ -440,7 +445,7 @@ cudaError_t launch_quant_fp4(const QuantJob* jobs, int njobs, int64_t n, int32_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quant_kernel, qj, n, static_cast<const int32_t*>(ws), parts);
+  return cudaLaunchKernelEx(&cfg, quant_kernel, qj, n, static_cast<const int32_t*>(ws), stride, (int)parts);
 }
 
 

@@ -205,7 +205,7 @@ cudaError_t store_chunk(kvc_cache* c, const void* k, const void* v, int32_t r, c
   const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
   QuantJob jobs[2] = {{k, static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r},
                       {v, static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r}};
-  return launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, st);
+  return launch_quant_fp4(jobs, 2, n, c->dev_ws + 1, KVC_WS_WORDS - 1, st);
 }
 
 // State check of an append of chunk_idx (as a new shot's sink when `shot`):
@@ -427,13 +427,20 @@ int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const fl
   rl.dev_err = c->dev_ws;
   cudaError_t e = launch_recache(rl, st);
   if (e != cudaSuccess || !fp4) return cuda_status(e);
+  // every region's K and V encoded as its own tensor, all in one encode (two launches)
+  QuantJob jobs[kMaxQuantJobs];
+  const int64_t Tc = chunk_tokens(c);
   for (int i = 0; i < n; ++i) {
-    const uint8_t* ks = static_cast<const uint8_t*>(rl.k) + (size_t)i * hd2;
-    const uint8_t* vs = static_cast<const uint8_t*>(rl.v) + (size_t)i * hd2;
-    e = store_chunk(c, ks, vs, region_of(c, chunk_ids[i]), st);
-    if (e != cudaSuccess) return KVC_ECUDA;
+    const int32_t r = region_of(c, chunk_ids[i]);
+    const size_t coff = (size_t)r * Tc * row_bytes(c, 0);
+    const size_t soff = (size_t)r * Tc * row_bytes(c, 2);
+    jobs[2 * i] = QuantJob{static_cast<const uint8_t*>(rl.k) + (size_t)i * hd2,
+                           static_cast<uint8_t*>(c->k) + coff, c->k_scale + soff, c->k_gscale + r};
+    jobs[2 * i + 1] = QuantJob{static_cast<const uint8_t*>(rl.v) + (size_t)i * hd2,
+                               static_cast<uint8_t*>(c->v) + coff, c->v_scale + soff, c->v_gscale + r};
   }
-  return KVC_OK;
+  e = launch_quant_fp4(jobs, 2 * n, Tc * c->heads * (int64_t)c->head_dim, c->dev_ws + 1, KVC_WS_WORDS - 1, st);
+  return e == cudaSuccess ? KVC_OK : KVC_ECUDA;
 }
 
 int32_t kvc_project_append(kvc_cache* c, const void* hidden, const void* w_qkv,
@@ -497,7 +504,7 @@ int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
       (reinterpret_cast<uintptr_t>(gscale) & 3u) || (reinterpret_cast<uintptr_t>(ws) & 3u))
     return KVC_EINVAL;
   QuantJob job{x, codes, scales, gscale};
-  return cuda_status(launch_quant_fp4(&job, 1, n, ws, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_quant_fp4(&job, 1, n, ws, KVC_QUANT_WS_WORDS, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream) {

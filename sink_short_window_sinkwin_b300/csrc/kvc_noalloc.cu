@@ -58,7 +58,7 @@ extern "C" int32_t kvc_quant_fp4_noalloc(const void* x, int64_t n, uint8_t* code
   // The first pass writes every one of its kQuantPartials words before the
   // second pass reads them, so nothing has to be cleared between calls.
   QuantJob job{x, codes, scales, gscale};
-  return launch_quant_fp4(&job, 1, n, scratch, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_quant_fp4(&job, 1, n, scratch, kQuantPartials, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? KVC_OK
              : KVC_ECUDA;
