@@ -154,6 +154,34 @@ def test_recache_layer_full_size_then_attention(swl):
     assert cache.last_device_error() == swl.KVC_OK
 
 
+def test_recache_layer_graph_capture_matches_eager(swl):
+    """At the LongLive-1.3B shape the recache is two launches on two streams
+    (3-CTA clusters, and the SMs no cluster fits taking some V items), forked
+    from and joined back to the caller's stream with events.  Captured into a
+    CUDA graph and replayed onto a scrubbed cache, it must write exactly what
+    the eager call wrote."""
+    sh = LAYER_1P3B
+    cache, model = _fill(swl, sh, 3)
+    ids = model.present_chunks()
+    hid, wkv, gamma = recache_inputs(sh, 5, len(ids))
+    hid, wkv, gamma = hid.cuda(), wkv.cuda(), gamma.cuda()
+    cache.recache(hid, wkv, gamma, ids, sh.grid_h, sh.grid_w)
+    torch.cuda.synchronize()
+    k0, v0 = cache.k.clone(), cache.v.clone()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        cache.recache(hid, wkv, gamma, ids, sh.grid_h, sh.grid_w)
+    cache.k.fill_(float("nan"))
+    cache.v.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(cache.k.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(cache.v.view(torch.int16), v0.view(torch.int16))
+    assert cache.last_device_error() == swl.KVC_OK
+
+
 def test_recache_equals_appended_projections(swl):
     """Recache => append consistency on the GPU: stream chunks 0..6 whose K/V
     are the oracle's per-chunk projections (project_chunk: norm + 3D RoPE at
