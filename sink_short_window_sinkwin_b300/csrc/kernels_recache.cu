@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(kNormWarps * 32) recache_norm_rope_kernel(cons
 // items are (row tile, K or V): item i is row tile i / 2, K for even i, and the
 // clusters take items in turn, so the K and V items of a row tile run on
 // neighbouring clusters at about the same time and share the hidden rows
-// through L2.  K item epilogue: every thread sums the squares of its row over
+// through L2.  The SMs that no cluster fits on run a second, cluster-free
+// launch of the same kernel that takes the V items of the last row tiles
+// (FusedParams::vonly).  K item epilogue: every thread sums the squares of its row over
 // its 256 columns and stores that partial into every CTA of the cluster (its
 // own included) before a release-arrive on the receiver's exchange barrier;
 // with all 2 * HD / 512 partials of its rows in hand (summed in slot order, so
