@@ -205,12 +205,19 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq,
  * (P - 2*(P/3), P/3, P/3) pairs, P = D/2; in a band of b dims pair j turns by
  * position * rope_theta^(-2j/b).  grid_h * grid_w == tokens_per_frame.
  * H*D in {64, 128, 256, 512, 768, 1024, 1536, 2048, 3072} (else KVC_EUNSUPPORTED).
- * bf16 cache: three launches on `stream` (K projection, norm + RoPE, V
- * projection); between them the regions being rebuilt hold intermediate values,
- * so nothing may read those regions until the stream passes the call.
- * FP4 cache: the same three launches write bf16 K and V of all n chunks into
- * `stage` (n * Tc * H*D * 4 bytes needed, else KVC_EINVAL), then each region is
- * FP4-encoded from them with kvc_quant_fp4's rule (its own tensor scale).
+ * bf16 cache: H*D a multiple of 512 up to 2048 with D in {64, 128}: one fused
+ * launch on `stream` (K and V projections, the norm and rotation applied to K
+ * before it is written), plus, when the SMs do not divide into its thread-block
+ * clusters, a second launch on a library-owned side stream that waits for the
+ * work already in `stream` and that `stream` waits for (event fork and join;
+ * this holds under stream capture).  Other shapes: three launches on `stream`
+ * (K projection, norm + RoPE, V projection), between which the regions being
+ * rebuilt hold intermediate values.  Either way nothing may read those regions
+ * until the stream passes the call.
+ * FP4 cache: the same launches write bf16 K and V of all n chunks into `stage`
+ * (n * Tc * H*D * 4 bytes needed, else KVC_EINVAL), then every region's K and V
+ * are FP4-encoded from them with kvc_quant_fp4's rule, each its own tensor
+ * with its own tensor scale (one encode over all of them).
  * Defined by: LongLive summary page, 方法 §1 KV 重缓存 (at the switch the cache is
  * recomputed from the generated frames with the new prompt); FP4 store: LongLive
  * 2.0 inference blog, "NVFP4 量化与 KV Cache 压缩的工程实现". */

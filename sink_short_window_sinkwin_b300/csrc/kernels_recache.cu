@@ -11,8 +11,11 @@
 //
 // RMSNorm spans the whole H*D-wide row, which no single 128 x 256 output tile
 // holds, and rounding to bf16 before the norm and again after it would round
-// twice.  So the GEMM stores the rows to be normalised as fp32 ("parked"), and
-// a second launch normalises them:
+// twice.  The recache at H*D = 512 .. 2048 in steps of 512 (D 64 or 128) is the
+// fused kernel further down: a thread-block cluster holds a whole row in TMEM
+// and exchanges the per-row sums of squares through distributed shared memory.
+// Other shapes, and the chunk projection, store the rows to be normalised as
+// fp32 ("parked") and a second launch normalises them:
 //   recache into a bf16 cache (three stream-ordered launches):
 //   1. K GEMM: the unnormalised fp32 K row of token `dest` is parked in the
 //      cache's own K and V rows of that token (each row is H*D*2 bytes, so the
