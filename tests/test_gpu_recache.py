@@ -122,6 +122,20 @@ def test_recache_fused_rotation_paths(swl, shape):
     _compare_cache(cache, model, sh, what=f"fused rotation paths {shape}")
 
 
+def test_recache_side_launch_four_cta_clusters(swl):
+    """H*D = 2048: clusters of 4 CTAs (33 fit on 148 SMs), so the 16 SMs left
+    take the V items of the last row tiles in the cluster-free launch; 4 chunks
+    of 1280 rows (40 row tiles) make that split non-empty.  Sampled rows of
+    every region, both launches' row tiles among them."""
+    sh = Shapes(16, 128, 640, 2, 3, 10, 64)
+    cache, model = _fill(swl, sh, 3)
+    assert model.present_chunks() == [0, 1, 2, 3]
+    _recache_both(swl, sh, cache, model, 29, gamma_rand=True)
+    rows = [0, 1, 127, 128, 640, 1023, 1024, 1151, 1152, 1279]
+    _compare_cache(cache, model, sh, rows=rows, what="H*D=2048 side launch")
+    assert cache.last_device_error() == swl.KVC_OK
+
+
 @pytest.mark.parametrize("heads,head_dim", [(1, 128), (2, 128), (6, 128)])
 def test_recache_tile_widths(swl, heads, head_dim):
     """H*D = 128, 256, 768: GEMM column tiles 128 or 256 wide (one, one and three
