@@ -62,7 +62,7 @@ TRAFFIC = {
     "sinkwin_attn_kernel<128,true>": {"bytes": 47181056 + 4062208, "src_sha": "b4ae518685bd2dfc"},
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
-    "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "491fef69fdc1c5a3"},
+    "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
 }
 
 

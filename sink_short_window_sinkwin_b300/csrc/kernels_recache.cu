@@ -809,12 +809,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
         float tot = 0.0f;
         for (int s2 = 0; s2 < 2 * ncta; ++s2) tot += sm.exch[buf][s2][rloc];
         const float rstd = 1.0f / sqrtf(tot / (float)p.HD + p.eps);
-        // pass 2: chunk i at column (i / npc) * D + (i % npc) * 32 (head-major),
-        // two adjacent chunks (64 columns, whole 128-byte rows of output) per
-        // TMEM wait; rstd rides on cos and sin
+        // pass 2: x * gamma, rotated, rstd riding on cos and sin
         const int nch = npc * nh;
         tmem_ld32(tq, xa);
-        tmem_ld32(tq + 32u, xb);
+        tmem_ld32(tq + (uint32_t)p.D, xb);
         // {cos, sin} * rstd of the 16 rotation pairs of pair chunk pc
         auto rotations = [&](int pc, float (&cs)[16], float (&sn)[16]) {
           if (fh_tab && p.w_tab) {  // every rotation from a table (warp-uniform)
@@ -843,32 +841,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
           }
         };
+        // chunk i at column (i % nh) * D + (i / nh) * 32: the nh chunks of a
+        // pair chunk (the same 16 rotations in every head) in turn, two per
+        // TMEM wait, so each pair chunk's rotations are looked up once
+        float cs[16], sn[16];
 #pragma unroll 1
         for (int i = 0; i < nch; i += 2) {
-          const int pc = i % npc;  // even: chunks pc and pc + 1 of head i / npc
-          const int cola = (i / npc) * p.D + pc * 32;
+          const int pc = i / nh;
+          if (i % nh == 0) rotations(pc, cs, sn);
+          const int cola = (i % nh) * p.D + pc * 32;
+          const int colb = cola + p.D;  // chunk i + 1: the next head, same pair chunk
           const int i2 = i + 2;
-          const uint32_t c2 = (uint32_t)((i2 / npc) * p.D + (i2 % npc) * 32);  // next pair's first column
+          const uint32_t c2 = (uint32_t)((i2 % nh) * p.D + (i2 / nh) * 32);  // next pair's first column
           uint32_t wa[16], wb[16];
-          {
-            float cs[16], sn[16];
-            rotations(pc, cs, sn);
-            tmem_ld_wait();
-            rope_pack(xa, gam + cola, cs, sn, wa);
-          }
+          tmem_ld_wait();
+          rope_pack(xa, gam + cola, cs, sn, wa);
           if (i2 < nch) tmem_ld32(tq + c2, xa);
-          {
-            float cs[16], sn[16];
-            rotations(pc + 1, cs, sn);
-            rope_pack(xb, gam + cola + 32, cs, sn, wb);
-          }
-          if (i2 < nch) tmem_ld32(tq + c2 + 32u, xb);
+          rope_pack(xb, gam + colb, cs, sn, wb);
+          if (i2 < nch) tmem_ld32(tq + c2 + (uint32_t)p.D, xb);
           if (p.tma_out) {
             stage_store_bulk(stg, wa, tmo32, tmo, gcol0 + cola, d8, ngroups, whole, lane);
-            stage_store_bulk(stg, wb, tmo32, tmo, gcol0 + cola + 32, d8, ngroups, whole, lane);
+            stage_store_bulk(stg, wb, tmo32, tmo, gcol0 + colb, d8, ngroups, whole, lane);
           } else {
             stage_store16(stg, wa, obase + cola / 8, ld, my_dest, row0, p.rows, lane);
-            stage_store16(stg, wb, obase + cola / 8 + 4, ld, my_dest, row0, p.rows, lane);
+            stage_store16(stg, wb, obase + colb / 8, ld, my_dest, row0, p.rows, lane);
           }
         }
       } else {
@@ -1082,12 +1078,12 @@ cudaError_t launch_recache_fused(const RecacheLaunch& r, cudaStream_t st) {
   // SMs that no cluster fits on (13 of 148 for 3-CTA clusters) take the V
   // items of the last x row tiles in a second, cluster-free launch beside the
   // first: x balances the two by the measured item costs (a K item, with its
-  // norm and rotation epilogue, takes about 1.43 times a V item)
+  // norm and rotation epilogue, takes about 1.35 times a V item)
   const int nsm = attn_sm_count();
   const int nfree = nsm - ncl * ncta;
   int x = 0;
   if (nfree > 0) {
-    constexpr double kCostK = 1.43, kCostV = 1.0;
+    constexpr double kCostK = 1.35, kCostV = 1.0;
     double best = (nrt * kCostK + nrt * kCostV) / ncl;
     for (int xx = 1; xx <= nrt; ++xx) {
       const double ta = (nrt * kCostK + (nrt - xx) * kCostV) / ncl;
