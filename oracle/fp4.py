@@ -144,3 +144,17 @@ def dequantize(packed: np.ndarray, scales: np.ndarray, g) -> np.ndarray:
     s = np.repeat(s, F4_BLOCK, axis=-1)
     assert s.shape[-1] == D
     return vals * s * float(np.float32(g))
+
+
+def gemm_dequantized(a_codes, a_scales, a_g, b_codes, b_scales, b_g) -> np.ndarray:
+    """W4A4 projection: dequantize(A) @ dequantize(B), exact products summed in
+    float64.
+
+    LongLive 2.0 inference blog (blog.hotdry.top), "NVFP4 量化与 KV Cache 压缩的
+    工程实现": NVFP4 (W4A4) inference keeps both weights and activations in 4-bit
+    floating point; the NVIDIA infrastructure blog (bittide page), §6, lists
+    W4A4 execution in the LongLive 2.0 system.  A (activations) is [M][K] and
+    B (the weight, one row per output feature) is [N][K]; each is an FP4
+    tensor of this module's format, its 16-element blocks along K, one fp32
+    tensor scale.  The result is [M][N] = deq(A) deq(B)^T."""
+    return dequantize(a_codes, a_scales, a_g) @ dequantize(b_codes, b_scales, b_g).T

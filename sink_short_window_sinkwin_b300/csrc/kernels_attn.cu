@@ -222,25 +222,6 @@ __device__ __forceinline__ Share share_of(const AttnParams& p, int g) {
 // FP4 tile dequantisation: thread i writes key row i of a K or V tile in the
 // 128-byte-swizzled layout the MMA descriptors expect.
 // ---------------------------------------------------------------------------
-// 8 E2M1 codes (4 bytes, element 2i in the low nibble of byte i) -> 4 f16x2
-__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t word, uint32_t (&d)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-      : "r"(word));
-}
-// two E4M3 block scales (low byte first) -> f16x2 (exact: E4M3 values lie in
-// the f16 normal range)
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(two_bytes));
-  return d;
-}
-
 // One key row of FP4 codes and block scales, held in registers so the loads
 // for the next tile can be in flight while this one is decoded.
 template <int D>

@@ -198,3 +198,54 @@ def test_tiny_tensor_blocks_without_finite_reciprocal():
     err = np.abs(xh - x.astype(np.float64))
     assert np.all(err[live] <= sv[live][:, None] * 1.0)
     assert np.all(xh[x == 0] == 0)
+
+
+def test_gemm_dequantized_against_loops():
+    """The W4A4 projection against a triple loop written from the format's
+    value tables (code -> E2M1 value, scale byte -> E4M3 value, times g)."""
+    rng = np.random.default_rng(17)
+    M, K, N = 5, 32, 48
+    a = (rng.standard_normal((M, K)) * rng.uniform(0.1, 3.0, (M, 1))).astype(np.float32)
+    b = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    ac, as_, ag = fp4.quantize(a)
+    bc, bs, bg = fp4.quantize(b)
+    got = fp4.gemm_dequantized(ac, as_, ag, bc, bs, bg)
+
+    def value(codes, scales, g, r, c):
+        byte = int(codes[r, c // 2])
+        code = byte & 0xF if c % 2 == 0 else byte >> 4
+        return fp4.e2m1_value(code) * fp4.e4m3_value(int(scales[r, c // 16])) * float(g)
+
+    want = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            want[i, j] = sum(value(ac, as_, ag, i, k) * value(bc, bs, bg, j, k) for k in range(K))
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+def test_gemm_dequantized_exact_on_representable_inputs():
+    """Inputs already on the FP4 grid come back unchanged, so the projection
+    equals the plain product of the inputs.  Each tensor's maximum is 2688
+    times a power of two (the tensor scale g is then a power of two) and each
+    block is E2M1 values times a block factor f whose f / g is an E4M3 value
+    (3.5 * 2^7 = 448, or a power of two)."""
+    rng = np.random.default_rng(3)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def on_grid(rows, cols, top):
+        x = rng.choice(grid, (rows, cols)) * rng.choice([-1, 1], (rows, cols))
+        x[:, ::16] = 6.0                       # every block maximum is 6 * f
+        f = 2.0 ** rng.integers(-2, 2, (rows, cols // 16))
+        f[0, 0] = top                          # the tensor maximum 6 * top
+        return x * np.repeat(f, 16, axis=1)
+
+    M, K, N = 4, 32, 32
+    a = on_grid(M, K, 1.75)                    # amax 10.5 = 2688 / 2^8
+    b = on_grid(N, K, 3.5)                     # amax 21 = 2688 / 2^7
+    ac, as_, ag = fp4.quantize(a.astype(np.float32))
+    bc, bs, bg = fp4.quantize(b.astype(np.float32))
+    assert float(ag) == 2.0 ** -8
+    assert float(bg) == 2.0 ** -7
+    assert np.array_equal(fp4.dequantize(ac, as_, ag), a)
+    assert np.array_equal(fp4.dequantize(bc, bs, bg), b)
+    assert np.array_equal(fp4.gemm_dequantized(ac, as_, ag, bc, bs, bg), a @ b.T)
