@@ -209,3 +209,32 @@ def quant_fp4(x: torch.Tensor, stream=None):
         check(lib().kvc_quant_fp4(_ptr(x), int(n), _ptr(codes), _ptr(scales), _ptr(g), _ptr(ws),
                                   _stream(dev, stream)), "kvc_quant_fp4")
     return codes, scales, g
+
+
+def gemm_fp4(a, b, M: int, N: int, K: int, out=None, dev_err=None, stream=None) -> torch.Tensor:
+    """W4A4 projection deq(A) deq(B)^T -> bf16 [M][N].  `a` and `b` are
+    (codes, scales, gscale) triples as quant_fp4 returns them: A's encode the
+    [M][K] activations, B's an [N][K] weight (one row per output feature);
+    codes u8 rows*K/2, scales u8 rows*K/16, gscale f32 [1], any contiguous
+    shape.  N % 256 == 0 and K % 256 == 0.  dev_err: optional int32 CUDA
+    tensor whose first word records a kernel timeout."""
+    (ac, as_, ag), (bc, bs, bg) = a, b
+    for t, name, n in ((ac, "a codes", M * K // 2), (as_, "a scales", M * K // 16),
+                       (bc, "b codes", N * K // 2), (bs, "b scales", N * K // 16)):
+        if (t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous()
+                or t.numel() != n):
+            raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor of {n} bytes")
+    for t, name in ((ag, "a gscale"), (bg, "b gscale")):
+        if t.dtype != torch.float32 or not t.is_cuda or t.numel() != 1:
+            raise ValueError(f"{name} must be a CUDA float32 tensor of one element")
+    if dev_err is not None and (dev_err.dtype != torch.int32 or not dev_err.is_cuda):
+        raise ValueError("dev_err must be a CUDA int32 tensor")
+    dev = _cuda_device(ac.device)
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=ac.device)
+    _require(out, torch.bfloat16, (M, N), "out", ac.device)
+    with torch.cuda.device(dev):
+        check(lib().kvc_gemm_fp4(_ptr(ac), _ptr(as_), _ptr(ag), _ptr(bc), _ptr(bs), _ptr(bg),
+                                 int(M), int(N), int(K), _ptr(out), _ptr(dev_err),
+                                 _stream(dev, stream)), "kvc_gemm_fp4")
+    return out

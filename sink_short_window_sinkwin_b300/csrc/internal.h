@@ -120,6 +120,21 @@ cudaError_t set_smem_once(K kern, size_t bytes, bool (&done)[64]) {
   return e;
 }
 
+// ---- W4A4 projection (FP4 x FP4 -> bf16) ----
+struct GemmFp4Launch {
+  const uint8_t* a_codes;   // [M][K/2]
+  const uint8_t* a_scales;  // [M][K/16]
+  const float* a_gscale;    // device [1]
+  const uint8_t* b_codes;   // [N][K/2]
+  const uint8_t* b_scales;  // [N][K/16]
+  const float* b_gscale;    // device [1]
+  int64_t M, N, K;          // N % 256 == 0, K % 256 == 0
+  void* out;                // bf16 [M][N]
+  int32_t* dev_err;         // may be null
+};
+cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st);
+size_t gemm_fp4_smem_bytes();
+
 // ---- diagnostics ----
 cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st);
 
@@ -132,5 +147,9 @@ bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
 // the same with a swizzle of 0, 32, 64 or 128 bytes
 bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                             uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes);
+// 2D tensor of bytes (d0 innermost), swizzle of 0, 32, 64 or 128 bytes; rows
+// past d1 read as zero
+bool encode_tmap_2d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes);
 
 }  // namespace kvc

@@ -53,8 +53,9 @@ bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
   return encode_tmap_2d_bf16_sw(m, base, d0, d1, stride1_bytes, box0, box1, swizzle128 ? 128 : 0);
 }
 
-bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
-                            uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes) {
+static bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0,
+                           uint64_t d1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                           int swizzle_bytes) {
   CUtensorMapSwizzle sw;
   switch (swizzle_bytes) {
     case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
@@ -69,10 +70,22 @@ bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint6
   cuuint64_t strides[1] = {stride1_bytes};
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_2d_bf16_sw(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                            uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d0, d1, stride1_bytes, box0, box1,
+                        swizzle_bytes);
+}
+
+bool encode_tmap_2d_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                       uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle_bytes) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, d0, d1, stride1_bytes, box0, box1,
+                        swizzle_bytes);
 }
 
 // ---------------------------------------------------------------------------
@@ -505,6 +518,26 @@ int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
     return KVC_EINVAL;
   QuantJob job{x, codes, scales, gscale};
   return cuda_status(launch_quant_fp4(&job, 1, n, ws, KVC_QUANT_WS_WORDS, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvc_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_gscale,
+                     const uint8_t* b_codes, const uint8_t* b_scales, const float* b_gscale,
+                     int64_t M, int64_t N, int64_t K, void* out, int32_t* dev_err,
+                     kvc_stream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31))
+    return KVC_EINVAL;
+  if (M == 0) return KVC_OK;  // an empty product: no pointer is read
+  if (!a_codes || !a_scales || !a_gscale || !b_codes || !b_scales || !b_gscale || !out)
+    return KVC_EINVAL;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(b_codes) || !aligned16(b_scales) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(a_gscale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(b_gscale) & 3u) || (reinterpret_cast<uintptr_t>(dev_err) & 3u))
+    return KVC_EINVAL;
+  if (N % 256 != 0 || K % 256 != 0) return KVC_EUNSUPPORTED;
+  if (((M + 127) / 128) * (N / 256) >= (int64_t(1) << 31)) return KVC_EUNSUPPORTED;
+  GemmFp4Launch g{a_codes, a_scales, a_gscale, b_codes, b_scales, b_gscale, M, N, K, out, dev_err};
+  return cuda_status(launch_gemm_fp4(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t kvc_last_device_error(const kvc_cache* c, kvc_stream_t stream) {

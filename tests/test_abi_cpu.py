@@ -129,6 +129,23 @@ def test_quant_and_watchdog_validation(lib):
     assert lib.kvc_quant_fp4(x, 15, x, x, x, x, None) == _abi.KVC_EINVAL
     assert lib.kvc_quant_fp4(x, 0, x, x, x, x, None) == _abi.KVC_EINVAL
     assert lib.kvc_quant_fp4(None, 32, x, x, x, x, None) == _abi.KVC_EINVAL
+    # W4A4 projection: pointers, alignment and sizes are checked before any
+    # launch; M = 0 returns at once
+    g = ctypes.c_void_p(0x10000004)
+    ok = (x, x, g, x, x, g)
+    assert lib.kvc_gemm_fp4(*ok, 0, 256, 256, x, None, None) == _abi.KVC_OK
+    assert lib.kvc_gemm_fp4(None, None, None, None, None, None, 0, 256, 256, None, None,
+                            None) == _abi.KVC_OK
+    assert lib.kvc_gemm_fp4(None, x, g, x, x, g, 4, 256, 256, x, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, None, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, -1, 256, 256, x, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 0, 256, x, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, ctypes.c_void_p(0x10000008), None,
+                            None) == _abi.KVC_EINVAL                   # out not 16-byte aligned
+    assert lib.kvc_gemm_fp4(x, x, ctypes.c_void_p(0x10000002), x, x, g, 4, 256, 256, x, None,
+                            None) == _abi.KVC_EINVAL                   # gscale not 4-byte aligned
+    assert lib.kvc_gemm_fp4(*ok, 4, 128, 256, x, None, None) == _abi.KVC_EUNSUPPORTED
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 128, x, None, None) == _abi.KVC_EUNSUPPORTED
     assert lib.kvc_watchdog_selftest(None, 10, None) == _abi.KVC_EINVAL
     assert lib.kvc_watchdog_selftest(x, 0, None) == _abi.KVC_EINVAL
     assert lib.kvc_status_string(_abi.KVC_ESTATE).decode().startswith("invalid in")
