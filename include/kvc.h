@@ -289,22 +289,28 @@ int32_t kvc_quant_fp4_noalloc(const void* x, int64_t n, uint8_t* codes, uint8_t*
  *                     b_codes [N][K/2], b_scales [N][K/16], b_gscale [1], likewise
  *   out:              device bf16 [M][N], row-major; written, never read
  *   deq(x)[r][k] = e2m1(code) * e4m3(scale of block k/16) * gscale.
- * Each element product is exact in fp32 (the decoded values have at most 6
- * significant bits); the sums are fp32 (tensor-core accumulation order), then
- * scaled by a_gscale * b_gscale and rounded to bf16.  dev_err: optional device
- * int32 word (NULL: none) that records KVC_ETIMEOUT's cause if a kernel wait
- * runs out, as the cache's device error word does.
- * M >= 0 (0: KVC_OK at once, no pointer read), N and K > 0 and < 2^31; N % 256 != 0 or
- * K % 256 != 0: KVC_EUNSUPPORTED.  Codes, scales and out 16-byte aligned, the
- * gscales and dev_err 4-byte aligned, else KVC_EINVAL.  The call's kernel holds
- * all of an SM's tensor memory while it runs.
+ * Each decoded element and each product of two is exact (at most 6 significant
+ * bits); the sums are fp32 (tensor-core accumulation order), then scaled by
+ * a_gscale * b_gscale and rounded to bf16.
+ * ws: NULL, or device scratch of at least KVC_GEMM_FP4_WS_BYTES(M, N, K) bytes
+ * (ws_bytes) that the call overwrites.  NULL: one kernel decodes the FP4
+ * operands tile by tile inside the GEMM.  Given: A and B are decoded once into
+ * ws as f16 and a second kernel multiplies those (faster on this GPU; same
+ * result bits, the accumulation order aside).
+ * dev_err: optional device int32 word (NULL: none) that records KVC_ETIMEOUT's
+ * cause if a kernel wait runs out, as the cache's device error word does.
+ * M >= 0 (0: KVC_OK at once, no pointer read), N and K > 0 and < 2^31; N % 32 != 0 or
+ * K % 256 != 0: KVC_EUNSUPPORTED.  Codes, scales, out and ws 16-byte aligned, the
+ * gscales and dev_err 4-byte aligned, a short ws: KVC_EINVAL.  The call's
+ * kernels hold all of an SM's tensor memory while they run.
  * Defined by: LongLive 2.0 inference blog (blog.hotdry.top), "NVFP4 量化与 KV
  * Cache 压缩的工程实现" (NVFP4 W4A4: weights and activations both FP4); NVIDIA
  * infrastructure blog (bittide page), §6 (W4A4 execution in LongLive 2.0). */
+#define KVC_GEMM_FP4_WS_BYTES(M, N, K) ((((int64_t)(M)) + ((int64_t)(N))) * ((int64_t)(K)) * 2)
 int32_t kvc_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_gscale,
                      const uint8_t* b_codes, const uint8_t* b_scales, const float* b_gscale,
-                     int64_t M, int64_t N, int64_t K, void* out, int32_t* dev_err,
-                     kvc_stream_t stream);
+                     int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
+                     int32_t* dev_err, kvc_stream_t stream);
 
 /* Synchronise `stream`, read and clear the cache's device error word.
  * KVC_OK, KVC_ETIMEOUT (a kernel wait ran out), or KVC_ECUDA (a sticky CUDA error). */

@@ -57,7 +57,8 @@ SIGNATURES = {
                                   _i64, _i32, _i32, _i32, ctypes.c_float, _vp, _vp]),
     "kvc_quant_fp4": (_i32, [_vp, _i64, _vp, _vp, _vp, _vp, _vp]),
     "kvc_quant_fp4_noalloc": (_i32, [_vp, _i64, _vp, _vp, _vp, _vp]),
-    "kvc_gemm_fp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "kvc_gemm_fp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp,
+                            ctypes.c_size_t, _vp, _vp]),
     "kvc_last_device_error": (_i32, [ctypes.POINTER(KvcCache), _vp]),
     "kvc_watchdog_selftest": (_i32, [_vp, _i32, _vp]),
     "kvc_status_string": (ctypes.c_char_p, [_i32]),

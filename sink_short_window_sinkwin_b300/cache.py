@@ -211,13 +211,21 @@ def quant_fp4(x: torch.Tensor, stream=None):
     return codes, scales, g
 
 
-def gemm_fp4(a, b, M: int, N: int, K: int, out=None, dev_err=None, stream=None) -> torch.Tensor:
+def gemm_fp4_ws_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes of gemm_fp4's two-phase path (f16 copies of A and B)."""
+    return (M + N) * K * 2
+
+
+def gemm_fp4(a, b, M: int, N: int, K: int, out=None, ws=None, dev_err=None,
+             stream=None) -> torch.Tensor:
     """W4A4 projection deq(A) deq(B)^T -> bf16 [M][N].  `a` and `b` are
     (codes, scales, gscale) triples as quant_fp4 returns them: A's encode the
     [M][K] activations, B's an [N][K] weight (one row per output feature);
     codes u8 rows*K/2, scales u8 rows*K/16, gscale f32 [1], any contiguous
-    shape.  N % 256 == 0 and K % 256 == 0.  dev_err: optional int32 CUDA
-    tensor whose first word records a kernel timeout."""
+    shape.  N % 32 == 0 and K % 256 == 0.  ws: None (one fused kernel) or a
+    CUDA tensor of at least gemm_fp4_ws_bytes(M, N, K) bytes (decode once,
+    then an f16 GEMM).  dev_err: optional int32 CUDA tensor whose first word
+    records a kernel timeout."""
     (ac, as_, ag), (bc, bs, bg) = a, b
     for t, name, n in ((ac, "a codes", M * K // 2), (as_, "a scales", M * K // 16),
                        (bc, "b codes", N * K // 2), (bs, "b scales", N * K // 16)):
@@ -229,12 +237,17 @@ def gemm_fp4(a, b, M: int, N: int, K: int, out=None, dev_err=None, stream=None) 
             raise ValueError(f"{name} must be a CUDA float32 tensor of one element")
     if dev_err is not None and (dev_err.dtype != torch.int32 or not dev_err.is_cuda):
         raise ValueError("dev_err must be a CUDA int32 tensor")
+    ws_bytes = 0
+    if ws is not None:
+        if not ws.is_cuda or not ws.is_contiguous() or ws.device != ac.device:
+            raise ValueError("ws must be a contiguous CUDA tensor on the operands' device")
+        ws_bytes = ws.numel() * ws.element_size()
     dev = _cuda_device(ac.device)
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=ac.device)
     _require(out, torch.bfloat16, (M, N), "out", ac.device)
     with torch.cuda.device(dev):
         check(lib().kvc_gemm_fp4(_ptr(ac), _ptr(as_), _ptr(ag), _ptr(bc), _ptr(bs), _ptr(bg),
-                                 int(M), int(N), int(K), _ptr(out), _ptr(dev_err),
-                                 _stream(dev, stream)), "kvc_gemm_fp4")
+                                 int(M), int(N), int(K), _ptr(out), _ptr(ws), int(ws_bytes),
+                                 _ptr(dev_err), _stream(dev, stream)), "kvc_gemm_fp4")
     return out

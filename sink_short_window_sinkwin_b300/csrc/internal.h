@@ -128,12 +128,14 @@ struct GemmFp4Launch {
   const uint8_t* b_codes;   // [N][K/2]
   const uint8_t* b_scales;  // [N][K/16]
   const float* b_gscale;    // device [1]
-  int64_t M, N, K;          // N % 256 == 0, K % 256 == 0
+  int64_t M, N, K;          // N % 32 == 0, K % 256 == 0
   void* out;                // bf16 [M][N]
   int32_t* dev_err;         // may be null
+  void* ws;                 // null: fused kernel; else gemm_fp4_ws_bytes(M, N, K) bytes
 };
 cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st);
 size_t gemm_fp4_smem_bytes();
+int64_t gemm_fp4_ws_bytes(int64_t M, int64_t N, int64_t K);
 
 // ---- diagnostics ----
 cudaError_t launch_watchdog_selftest(int32_t* dev_ws, int32_t limit_us, cudaStream_t st);

@@ -11,17 +11,26 @@
 // Design.  Every E2M1 value times its E4M3 block scale has at most 6
 // significant bits and lies in [2^-10, 2688], so it is exact in f16; every
 // product of two such values is exact in fp32.  The kernel therefore decodes
-// the operands into f16 shared-memory tiles and multiplies them with the
-// kind::f16 tcgen05 MMA, fp32 accumulators in TMEM; the two tensor scales are
-// applied once to the accumulator.  The only roundings are the fp32
-// accumulation and the final bf16 conversion.
+// the operands to f16 and multiplies them with the kind::f16 tcgen05 MMA, fp32
+// accumulators in TMEM; the two tensor scales are applied once to the
+// accumulator.  The only roundings are the fp32 accumulation and the final
+// bf16 conversion.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over 128 x 256 tiles):
-//   warps 0-7   decode: raw FP4 stage (K = 256) -> four f16 stages (K = 64)
-//   warp 8      TMA: raw codes (128-byte swizzled) and scales of A and B
-//   warp 9      MMA issue (one thread): 4 x (128 x 256 x 16) per f16 stage
-//   warps 10-13 epilogue: TMEM -> x (g_a g_b) -> bf16 -> global
-// Every wait is bounded (the device error word records a timeout).
+// Shared-memory bandwidth is what limits a decode-in-the-loop GEMM: the MMA
+// reads its shared-memory operands at a large fraction of it already.  So the
+// decoded A tile goes to TMEM (tcgen05.st; the MMA takes A from TMEM) and
+// only B's decoded tile is written to and read from shared memory.
+//
+// Warp roles (512 threads, one CTA per SM, persistent over 128 x 192 tiles):
+//   warps 0-9   decode: raw FP4 stage (K = 256) -> four f16 stages (K = 64):
+//               A rows into TMEM, B rows into 128-byte swizzled shared memory
+//   warp 10     TMA: raw codes (128-byte swizzled) and scales of A and B
+//   warp 11     MMA issue (one thread): 4 x (128 x 192 x 16) per f16 stage
+//   warps 12-15 epilogue: TMEM -> x (g_a g_b) -> bf16 -> global
+// TMEM: two 192-column accumulators (columns 0-383) and two A stages of 32
+// columns (384-447).  The epilogue writes bf16 boxes of 32 x 32 through
+// shared memory with bulk tensor stores.  Every wait is bounded (the device error word records a
+// timeout).
 #include <cstdint>
 
 #include "internal.h"
@@ -32,19 +41,24 @@ namespace kvc {
 namespace {
 
 constexpr int GM = 128;   // rows of A per tile (TMEM lanes)
-constexpr int GN = 256;   // rows of B (output columns) per tile
+constexpr int GN = 192;   // rows of B (output columns) per tile
 constexpr int GKR = 256;  // K elements per raw stage
 constexpr int GKD = 64;   // K elements per decoded f16 stage (128 bytes a row)
-constexpr int kRawStages = 2;
+constexpr int kRawStages = 3;
 constexpr int kDecStages = 2;
-constexpr int kDecodeWarps = 8;
-constexpr int kTmaWarp = 8, kMmaWarp = 9;  // warps 10-13: epilogue
-constexpr int kGThreads = 32 * 14;
-constexpr uint32_t kTmemCols = 2 * GN;  // two accumulators
-constexpr int kRows = GM + GN;          // operand rows decoded per stage
-// (row, half of a decoded stage) tasks per decode thread
-constexpr int kTasks = kRows * 2 / (kDecodeWarps * 32);
-static_assert(kTasks * kDecodeWarps * 32 == kRows * 2, "decode tasks must divide evenly");
+constexpr int kDecodeWarps = 10;
+constexpr int kTmaWarp = 10, kMmaWarp = 11;  // warps 12-15: epilogue
+constexpr int kGThreads = 32 * 16;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = GN;             // accumulator b at columns b * GN
+constexpr uint32_t kACol0 = 2 * GN;           // A stage d at columns kACol0 + 32 d
+static_assert(kACol0 + kDecStages * 32 <= kTmemCols, "TMEM holds both accumulators and the A stages");
+// Warp-tasks of one decoded stage: 32 rows x one half (32 elements) each.
+// A: 4 row quarters x 2 halves = 8; B: GN / 32 x 2 = 12.  Warp w takes tasks
+// w and w + kDecodeWarps; A task u (< 8) covers rows 32 (u % 4) .., which is
+// the TMEM lane quarter warp u may access (u % 4 == w % 4).
+constexpr int kATasks = 8, kBTasks = 2 * GN / 32;
+static_assert(kATasks + kBTasks == 2 * kDecodeWarps, "two warp-tasks per decode warp");
 static_assert(GKR / GKD == 4, "a raw stage is four decoded stages");
 
 struct Fp4GemmSmem {
@@ -52,8 +66,9 @@ struct Fp4GemmSmem {
   uint8_t b_codes[kRawStages][GN * GKR / 2];
   uint8_t a_sc[kRawStages][GM * GKR / 16];  // [row][16 B]
   uint8_t b_sc[kRawStages][GN * GKR / 16];
-  uint8_t a_dec[kDecStages][GM * GKD * 2];  // f16 [row][64], 128-byte swizzled (MMA operand)
-  uint8_t b_dec[kDecStages][GN * GKD * 2];
+  uint8_t b_dec[kDecStages][GN * GKD * 2];  // f16 [row][64], 128-byte swizzled (MMA operand)
+  // epilogue staging: per warp two 32 x 32 bf16 boxes, 64-byte swizzled rows
+  uint32_t ostage[4][2][32][16];
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint64_t dec_full[kDecStages], dec_empty[kDecStages];
   uint64_t acc_full[2], acc_empty[2];
@@ -64,18 +79,15 @@ struct Fp4GemmSmem {
 constexpr uint32_t kRawBytes = (GM + GN) * (GKR / 2 + GKR / 16);
 
 struct Fp4GemmParams {
-  int32_t M, ntn, ntiles, nks;  // rows, column tiles, tiles, raw stages along K
-  int64_t ldc;                  // output row stride (elements)
-  __nv_bfloat16* c;
+  int32_t M, N, ntn, ntiles, nks;  // rows, columns, column tiles, tiles, raw stages along K
   const float* a_g;
   const float* b_g;
   int32_t* dev_err;
 };
 
-// Decode 32 elements (16 code bytes, two 16-element blocks) of operand row r
-// into chunks 4 half .. 4 half + 3 of its 128-byte row in the f16 tile.
-__device__ __forceinline__ void decode32(uint8_t* dec, int r, int half, uint4 codes,
-                                         uint32_t scale_pair) {
+// 32 elements (16 code bytes = two 16-element blocks, `scale_pair` their two
+// E4M3 scales in its low 16 bits) -> 16 f16x2 words in element order
+__device__ __forceinline__ void decode32(uint4 codes, uint32_t scale_pair, uint32_t (&o)[16]) {
   const uint32_t sp = e4m3x2_to_f16x2(scale_pair);
   const __half2 s2 = *reinterpret_cast<const __half2*>(&sp);
   const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
@@ -84,22 +96,71 @@ __device__ __forceinline__ void decode32(uint8_t* dec, int r, int half, uint4 co
     const __half2 sc = wi < 2 ? __low2half2(s2) : __high2half2(s2);
     uint32_t h4[4];
     e2m1x8_to_f16x8(w[wi], h4);
-    uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const __half2 hv = __hmul2(*reinterpret_cast<const __half2*>(&h4[k]), sc);  // exact
-      o[k] = *reinterpret_cast<const uint32_t*>(&hv);
+      o[wi * 4 + k] = *reinterpret_cast<const uint32_t*>(&hv);
     }
-    const int ch = half * 4 + wi;
-    *reinterpret_cast<uint4*>(dec + r * 128 + ((ch ^ (r & 7)) << 4)) =
-        make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// One decode warp-task: which operand, its first row and its half.
+struct DecTask {
+  bool is_a;
+  int row0;  // first of the 32 rows (within the operand's tile)
+  int half;  // elements 32 half .. 32 half + 31 of each decoded stage
+};
+__device__ __forceinline__ DecTask dec_task(int u) {
+  if (u < kATasks) return {true, 32 * (u % 4), u / 4};
+  const int v = u - kATasks;
+  return {false, 32 * (v % (GN / 32)), v / (GN / 32)};
+}
+
+// Slot of 16-byte piece c (0..3) of staging row r: the layout of a 64-byte
+// swizzled box; 8 lanes writing piece c of 8 consecutive rows hit 8 bank groups.
+__device__ __forceinline__ int ostage_slot(int r, int c) { return c ^ ((r >> 1) & 3); }
+
+// One warp's 32 accumulator rows of a 128 x GN tile -> x gs -> bf16, stored
+// as 32 x 32 boxes through two staging buffers (`nst` counts this warp's boxes
+// and picks the buffer).  Row quarters past M are skipped (partial ones are
+// clipped by the store), and so are column chunks past N.
+__device__ __forceinline__ void store_tile(const CUtensorMap* tmC, uint32_t (*stage)[32][16], uint32_t acc,
+                                           int m0, int n0, int M, int N, float gs, int wq, int lane,
+                                           int& nst) {
+  const uint32_t trow = acc + ((uint32_t)(wq * 32) << 16);
+  const int row0 = m0 + wq * 32;
+  const bool live = row0 < M;
+  const int nch = min(GN, N - n0) / 32;
+  uint32_t x[32];
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    tmem_ld32(trow + c * 32, x);  // warp-collective
+    tmem_ld_wait();
+    if (!live) continue;
+    uint32_t (*stg)[16] = stage[nst & 1];
+    if (lane == 0) bulk_wait_read<1>();  // this buffer's previous box has been read
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint4*>(&stg[lane][4 * ostage_slot(lane, e)]) = make_uint4(
+          pack_bf16x2(__uint_as_float(x[8 * e + 0]) * gs, __uint_as_float(x[8 * e + 1]) * gs),
+          pack_bf16x2(__uint_as_float(x[8 * e + 2]) * gs, __uint_as_float(x[8 * e + 3]) * gs),
+          pack_bf16x2(__uint_as_float(x[8 * e + 4]) * gs, __uint_as_float(x[8 * e + 5]) * gs),
+          pack_bf16x2(__uint_as_float(x[8 * e + 6]) * gs, __uint_as_float(x[8 * e + 7]) * gs));
+    fence_proxy_async_smem();  // the bulk copy reads what the generic stores wrote
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, &stg[0][0], n0 + c * 32, row0);
+      bulk_commit();
+    }
+    ++nst;
   }
 }
 
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmAc, const __grid_constant__ CUtensorMap tmAs,
                     const __grid_constant__ CUtensorMap tmBc, const __grid_constant__ CUtensorMap tmBs,
-                    const __grid_constant__ Fp4GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Fp4GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   Fp4GemmSmem& sm =
       *reinterpret_cast<Fp4GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -135,18 +196,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   if (warp < kDecodeWarps) {
     // ------------------------------------------------------------ decode
-    // Thread t owns tasks t + 256 i (i < 3): operand row id % 384 (A rows
-    // 0..127, then B rows), half id / 384 of every decoded stage.  A warp's
-    // lanes take 32 consecutive rows, so the swizzled loads and stores hit 8
-    // distinct 16-byte bank groups per quarter warp.
-    const int t = threadIdx.x;
-    int row[kTasks], half[kTasks];
-#pragma unroll
-    for (int i = 0; i < kTasks; ++i) {
-      const int id = t + i * kDecodeWarps * 32;
-      row[i] = id % kRows;
-      half[i] = id / kRows;
-    }
+    // Lanes take 32 consecutive rows, so the swizzled 16-byte loads and
+    // stores of a quarter warp hit 8 distinct bank groups.
+    const DecTask tk[2] = {dec_task(warp), dec_task(warp + kDecodeWarps)};
     int rs = 0, ds = 0;  // raw / decoded stages passed (ring positions)
     bool ok = true;
     for (int tile = cta; tile < p.ntiles && ok; tile += ncta) {
@@ -156,35 +208,46 @@ __global__ void __launch_bounds__(kGThreads, 1)
           ok = false;
           break;
         }
-        // the row's 16 scale bytes of this raw stage (one per 16 elements)
-        uint4 sc[kTasks];
+        // each task row's 16 scale bytes of this raw stage (one per 16 elements)
+        uint4 sc[2];
+        const uint8_t* cbase[2];
 #pragma unroll
-        for (int i = 0; i < kTasks; ++i) {
-          const int r = row[i];
-          sc[i] = r < GM ? *reinterpret_cast<const uint4*>(&sm.a_sc[s][r * 16])
-                         : *reinterpret_cast<const uint4*>(&sm.b_sc[s][(r - GM) * 16]);
+        for (int i = 0; i < 2; ++i) {
+          const int r = tk[i].row0 + lane;
+          sc[i] = *reinterpret_cast<const uint4*>(tk[i].is_a ? &sm.a_sc[s][r * 16] : &sm.b_sc[s][r * 16]);
+          cbase[i] = (tk[i].is_a ? sm.a_codes[s] : sm.b_codes[s]) + r * 128;
         }
+        const int sw = lane & 7;  // (row & 7): the rows of a task start at multiples of 32
 #pragma unroll 1
         for (int j = 0; j < GKR / GKD; ++j, ++ds) {
           const int d = ds % kDecStages;
+          uint4 codes[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i)  // 16-byte chunk 2 j + half of the raw row
+            codes[i] = *reinterpret_cast<const uint4*>(cbase[i] + (((2 * j + tk[i].half) ^ sw) << 4));
           if (ds >= kDecStages && !mbar_wait(&sm.dec_empty[d], ((ds / kDecStages) - 1) & 1, wd)) {
             ok = false;
             break;
           }
 #pragma unroll
-          for (int i = 0; i < kTasks; ++i) {
-            const int r = row[i];
-            const int cidx = j * 2 + half[i];  // 16-byte chunk of the raw row
-            const bool is_a = r < GM;
-            const int rr = is_a ? r : r - GM;
-            const uint8_t* src = is_a ? sm.a_codes[s] : sm.b_codes[s];
-            const uint4 codes =
-                *reinterpret_cast<const uint4*>(src + rr * 128 + ((cidx ^ (rr & 7)) << 4));
-            const uint32_t sw = j == 0 ? sc[i].x : j == 1 ? sc[i].y : j == 2 ? sc[i].z : sc[i].w;
-            decode32(is_a ? sm.a_dec[d] : sm.b_dec[d], rr, half[i], codes,
-                     sw >> (16 * half[i]));
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t scw = j == 0 ? sc[i].x : j == 1 ? sc[i].y : j == 2 ? sc[i].z : sc[i].w;
+            uint32_t o[16];
+            decode32(codes[i], scw >> (16 * tk[i].half), o);
+            if (tk[i].is_a) {
+              // lane = tile row; columns 16 half .. of the stage's 32 (two f16 a column)
+              tmem_st16(tmem + ((uint32_t)tk[i].row0 << 16) + kACol0 + 32 * d + 16 * tk[i].half, o);
+            } else {
+              uint8_t* dst = sm.b_dec[d] + (tk[i].row0 + lane) * 128;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(dst + (((4 * tk[i].half + c) ^ sw) << 4)) =
+                    make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            }
           }
-          fence_proxy_async_smem();  // the f16 tile is read by the tensor cores
+          tmem_st_wait();            // the A words are in TMEM
+          fence_proxy_async_smem();  // the B tile is read by the tensor cores
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.dec_full[d]);
         }
@@ -211,7 +274,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             break;
           }
           mbar_expect_tx(&sm.raw_full[s], kRawBytes);
-          // x coordinates in bytes: ks * 128 and ks * 16, multiples of 16
+          // x coordinates in bytes: ks * 128 and ks * 16, multiples of 16;
+          // rows past M or N read as zero
           tma_load_2d(sm.a_codes[s], &tmAc, &sm.raw_full[s], ks * (GKR / 2), m0);
           tma_load_2d(sm.b_codes[s], &tmBc, &sm.raw_full[s], ks * (GKR / 2), n0);
           tma_load_2d(sm.a_sc[s], &tmAs, &sm.raw_full[s], ks * (GKR / 16), m0);
@@ -235,7 +299,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int buf = jt & 1;
         if (jt >= 2 && !mbar_wait(&sm.acc_empty[buf], ((jt >> 1) - 1) & 1, wd)) break;
         tc_fence_after();
-        const uint32_t acc = tmem + (uint32_t)(buf * GN);
+        const uint32_t acc = tmem + (uint32_t)buf * kAccCols;
         const int nsteps = p.nks * (GKR / GKD);
         for (int kd = 0; kd < nsteps; ++kd, ++ds) {
           const int d = ds % kDecStages;
@@ -244,11 +308,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint32_t a_t = tmem + kACol0 + 32 * d;
 #pragma unroll
           for (int kk = 0; kk < GKD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(smem_u32(sm.a_dec[d]) + kk * 32, 0, 1024);
             const uint64_t bd = sdesc_sw128(smem_u32(sm.b_dec[d]) + kk * 32, 0, 1024);
-            mma_bf16_ss(acc, ad, bd, idesc, (kd > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(acc, a_t + kk * 8, bd, idesc, (kd > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&sm.dec_empty[d]);  // the decoders may overwrite the stage
         }
@@ -259,35 +323,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3;  // TMEM lane quarter: tile rows 32 wq .. 32 wq + 31
     const float gs = __ldg(p.a_g) * __ldg(p.b_g);
-    int jt = 0;
+    if (lane == 0) tma_prefetch_desc(&tmC);
+    int jt = 0, nst = 0;
     for (int tile = cta; tile < p.ntiles; tile += ncta, ++jt) {
       const int buf = jt & 1;
-      const int m0 = (tile / p.ntn) * GM, n0 = (tile % p.ntn) * GN;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.acc_full[buf], (jt >> 1) & 1, wd))) break;
       tc_fence_after();
-      const uint32_t trow = tmem + (uint32_t)(buf * GN) + ((uint32_t)(wq * 32) << 16);
-      const int grow = m0 + wq * 32 + lane;
-      uint4* dst = reinterpret_cast<uint4*>(p.c + (int64_t)grow * p.ldc + n0);
-      uint32_t x[32];
-#pragma unroll 1
-      for (int c = 0; c < GN / 32; ++c) {
-        tmem_ld32(trow + c * 32, x);  // warp-collective; only the stores are predicated
-        tmem_ld_wait();
-        if (grow < p.M) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[c * 4 + e] = make_uint4(
-                pack_bf16x2(__uint_as_float(x[8 * e + 0]) * gs, __uint_as_float(x[8 * e + 1]) * gs),
-                pack_bf16x2(__uint_as_float(x[8 * e + 2]) * gs, __uint_as_float(x[8 * e + 3]) * gs),
-                pack_bf16x2(__uint_as_float(x[8 * e + 4]) * gs, __uint_as_float(x[8 * e + 5]) * gs),
-                pack_bf16x2(__uint_as_float(x[8 * e + 6]) * gs, __uint_as_float(x[8 * e + 7]) * gs));
-        }
-      }
+      store_tile(&tmC, sm.ostage[warp & 3], tmem + (uint32_t)buf * kAccCols, (tile / p.ntn) * GM,
+                 (tile % p.ntn) * GN, p.M, p.N, gs, warp & 3, lane, nst);
       tc_fence_before();
       mbar_arrive(&sm.acc_empty[buf]);  // the MMA may reuse this accumulator
     }
+    if (lane == 0) bulk_wait_all();  // every box has left shared memory and landed
   }
 
   tc_fence_before();
@@ -299,11 +347,241 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Two-phase path (caller workspace): decode A and B once to f16, then a plain
+// f16 GEMM fed by TMA.  The decode is done (M + N) K times instead of once per
+// tile, which on this GPU is worth the round trip through L2.
+// ---------------------------------------------------------------------------
+constexpr int kDecThreads = 256;
+constexpr int kDecUnroll = 4;
+
+// Rows are contiguous, so group i (8 elements) of the flat tensor has its 4 code
+// bytes at 4 i, its scale byte at i / 2 and its 16 bytes of f16 at 16 i: a
+// warp's loads and stores are contiguous.  Each thread takes kDecUnroll groups
+// a pass, its loads issued before any use.  The f16 value is e2m1(code) *
+// e4m3(scale), exact; the tensor scale is left to the GEMM's epilogue.
+__global__ void __launch_bounds__(kDecThreads)
+    fp4_to_f16_kernel(const uint8_t* __restrict__ a_codes, const uint8_t* __restrict__ a_scales,
+                      __half* __restrict__ a_out, int64_t a_groups, const uint8_t* __restrict__ b_codes,
+                      const uint8_t* __restrict__ b_scales, __half* __restrict__ b_out, int64_t b_groups) {
+  const int64_t n = a_groups + b_groups;
+  const int64_t stride = (int64_t)gridDim.x * kDecThreads;
+  for (int64_t base = (int64_t)blockIdx.x * kDecThreads + threadIdx.x; base < n;
+       base += stride * kDecUnroll) {
+    uint32_t w[kDecUnroll], sc[kDecUnroll];
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int64_t id = base + u * stride;
+      w[u] = 0;
+      sc[u] = 0;
+      if (id < n) {
+        const bool is_a = id < a_groups;
+        const int64_t i = is_a ? id : id - a_groups;
+        w[u] = __ldg(reinterpret_cast<const uint32_t*>(is_a ? a_codes : b_codes) + i);
+        sc[u] = __ldg((is_a ? a_scales : b_scales) + (i >> 1));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int64_t id = base + u * stride;
+      if (id >= n) break;
+      const bool is_a = id < a_groups;
+      const int64_t i = is_a ? id : id - a_groups;
+      const uint32_t sp = e4m3x2_to_f16x2(sc[u]);  // low half: the scale
+      const __half2 s2 = __low2half2(*reinterpret_cast<const __half2*>(&sp));
+      uint32_t h4[4];
+      e2m1x8_to_f16x8(w[u], h4);
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 hv = __hmul2(*reinterpret_cast<const __half2*>(&h4[k]), s2);  // exact
+        o[k] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      reinterpret_cast<uint4*>(is_a ? a_out : b_out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+constexpr int kFStages = 4;
+constexpr int kFThreads = 32 * 6;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+struct F16GemmSmem {
+  uint8_t a[kFStages][GM * GKD * 2];  // f16 [128][64], 128-byte swizzled (TMA)
+  uint8_t b[kFStages][GN * GKD * 2];  // f16 [192][64]
+  uint32_t ostage[4][2][32][16];
+  uint64_t full[kFStages], empty[kFStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+__global__ void __launch_bounds__(kFThreads, 1)
+    gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Fp4GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  F16GemmSmem& sm =
+      *reinterpret_cast<F16GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const int nk = p.nks * (GKR / GKD);  // K / 64
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 128);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Watchdog wd{&sm.abort_flag, p.dev_err};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int issued = 0;
+      bool ok = true;
+      for (int tile = cta; tile < p.ntiles && ok; tile += ncta) {
+        const int m0 = (tile / p.ntn) * GM, n0 = (tile % p.ntn) * GN;
+        for (int kb = 0; kb < nk; ++kb, ++issued) {
+          const int s = issued % kFStages, u = issued / kFStages;
+          if (issued >= kFStages && !mbar_wait(&sm.empty[s], (u - 1) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.full[s], (GM + GN) * GKD * 2);
+          tma_load_2d(sm.a[s], &tmA, &sm.full[s], kb * GKD, m0);  // rows past M or N read as zero
+          tma_load_2d(sm.b[s], &tmB, &sm.full[s], kb * GKD, n0);
+        }
+      }
+      if (sm.abort_flag) {  // every copy started here lands before the CTA exits
+        for (int s = 0; s < kFStages; ++s) {
+          const int cnt = issued > s ? (issued - s + kFStages - 1) / kFStages : 0;
+          if (cnt) mbar_drain(&sm.full[s], (cnt - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(GM, GN, false, false);
+      int used = 0, jt = 0;
+      bool ok = true;
+      for (int tile = cta; tile < p.ntiles && ok; tile += ncta, ++jt) {
+        const int buf = jt & 1;
+        if (jt >= 2 && !mbar_wait(&sm.acc_empty[buf], ((jt >> 1) - 1) & 1, wd)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)buf * kAccCols;
+        for (int kb = 0; kb < nk; ++kb, ++used) {
+          const int s = used % kFStages;
+          if (!mbar_wait(&sm.full[s], (used / kFStages) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < GKD / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(smem_u32(sm.a[s]) + kk * 32, 0, 1024);
+            const uint64_t bd = sdesc_sw128(smem_u32(sm.b[s]) + kk * 32, 0, 1024);
+            mma_bf16_ss(acc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.empty[s]);  // frees the stage for the producer
+        }
+        if (ok) mma_commit(&sm.acc_full[buf]);
+      }
+      mma_commit(&sm.drain);  // every MMA issued above completes before TMEM is freed
+      mbar_drain(&sm.drain, 0);
+    }
+  } else {
+    const float gs = __ldg(p.a_g) * __ldg(p.b_g);
+    if (lane == 0) tma_prefetch_desc(&tmC);
+    int jt = 0, nst = 0;
+    for (int tile = cta; tile < p.ntiles; tile += ncta, ++jt) {
+      const int buf = jt & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.acc_full[buf], (jt >> 1) & 1, wd))) break;
+      tc_fence_after();
+      store_tile(&tmC, sm.ostage[warp & 3], tmem + (uint32_t)buf * kAccCols, (tile / p.ntn) * GM,
+                 (tile % p.ntn) * GN, p.M, p.N, gs, warp & 3, lane, nst);
+      tc_fence_before();
+      mbar_arrive(&sm.acc_empty[buf]);
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 size_t gemm_fp4_smem_bytes() { return sizeof(Fp4GemmSmem) + 1024; }
 
+int64_t gemm_fp4_ws_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
+
 cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st) {
+  CUtensorMap tmC;
+  if (!encode_tmap_2d_bf16_sw(&tmC, g.out, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.N * 2, 32, 32, 64))
+    return cudaErrorInvalidValue;
+  Fp4GemmParams p{};
+  p.M = (int32_t)g.M;
+  p.N = (int32_t)g.N;
+  p.ntn = (int32_t)((g.N + GN - 1) / GN);
+  const int64_t ntm = (g.M + GM - 1) / GM;
+  p.ntiles = (int32_t)(ntm * p.ntn);
+  p.nks = (int32_t)(g.K / GKR);
+  p.a_g = g.a_gscale;
+  p.b_g = g.b_gscale;
+  p.dev_err = g.dev_err;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static int sm_count[64] = {};  // per device, looked up once
+  if (!sm_count[dev] && cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const int nsm = sm_count[dev];
+  const int grid = (int)(p.ntiles < nsm ? p.ntiles : nsm);
+
+  if (g.ws) {
+    // two phases: FP4 -> f16 into the workspace ([M][K] then [N][K]), f16 GEMM.
+    // The tensor maps are typed bf16: TMA moves 2-byte elements either way.
+    __half* a16 = reinterpret_cast<__half*>(g.ws);
+    __half* b16 = a16 + g.M * g.K;
+    const int64_t a_groups = g.M * g.K / 8, b_groups = g.N * g.K / 8;
+    const int64_t need = (a_groups + b_groups + kDecThreads * kDecUnroll - 1) / (kDecThreads * kDecUnroll);
+    const int dgrid = (int)(need < (int64_t)nsm * 8 ? need : (int64_t)nsm * 8);
+    fp4_to_f16_kernel<<<dgrid, kDecThreads, 0, st>>>(g.a_codes, g.a_scales, a16, a_groups, g.b_codes,
+                                                     g.b_scales, b16, b_groups);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmA, tmB;
+    if (!encode_tmap_2d_bf16_sw(&tmA, a16, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K * 2, GKD, GM, 128) ||
+        !encode_tmap_2d_bf16_sw(&tmB, b16, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.K * 2, GKD, GN, 128))
+      return cudaErrorInvalidValue;
+    const size_t smem = sizeof(F16GemmSmem) + 1024;
+    static bool done16[64] = {};
+    e = set_smem_once(gemm_f16_kernel, smem, done16);
+    if (e != cudaSuccess) return e;
+    gemm_f16_kernel<<<grid, kFThreads, smem, st>>>(tmA, tmB, tmC, p);
+    return cudaGetLastError();
+  }
+
   CUtensorMap tmAc, tmAs, tmBc, tmBs;
   const uint64_t kc = (uint64_t)g.K / 2, ksc = (uint64_t)g.K / 16;
   if (!encode_tmap_2d_u8(&tmAc, g.a_codes, kc, (uint64_t)g.M, kc, GKR / 2, GM, 128) ||
@@ -311,27 +589,11 @@ cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st) {
       !encode_tmap_2d_u8(&tmAs, g.a_scales, ksc, (uint64_t)g.M, ksc, GKR / 16, GM, 0) ||
       !encode_tmap_2d_u8(&tmBs, g.b_scales, ksc, (uint64_t)g.N, ksc, GKR / 16, GN, 0))
     return cudaErrorInvalidValue;
-  Fp4GemmParams p{};
-  p.M = (int32_t)g.M;
-  p.ntn = (int32_t)(g.N / GN);
-  const int64_t ntm = (g.M + GM - 1) / GM;
-  p.ntiles = (int32_t)(ntm * p.ntn);
-  p.nks = (int32_t)(g.K / GKR);
-  p.ldc = g.N;
-  p.c = reinterpret_cast<__nv_bfloat16*>(g.out);
-  p.a_g = g.a_gscale;
-  p.b_g = g.b_gscale;
-  p.dev_err = g.dev_err;
-
   const size_t smem = gemm_fp4_smem_bytes();
   static bool smem_done[64] = {};
   cudaError_t e = set_smem_once(gemm_fp4_kernel, smem, smem_done);
   if (e != cudaSuccess) return e;
-  int dev = 0, nsm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = (int)(p.ntiles < nsm ? p.ntiles : nsm);
-  gemm_fp4_kernel<<<grid, kGThreads, smem, st>>>(tmAc, tmAs, tmBc, tmBs, p);
+  gemm_fp4_kernel<<<grid, kGThreads, smem, st>>>(tmAc, tmAs, tmBc, tmBs, tmC, p);
   return cudaGetLastError();
 }
 

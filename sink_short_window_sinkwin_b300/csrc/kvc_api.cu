@@ -522,8 +522,8 @@ int32_t kvc_quant_fp4(const void* x, int64_t n, uint8_t* codes, uint8_t* scales,
 
 int32_t kvc_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_gscale,
                      const uint8_t* b_codes, const uint8_t* b_scales, const float* b_gscale,
-                     int64_t M, int64_t N, int64_t K, void* out, int32_t* dev_err,
-                     kvc_stream_t stream) {
+                     int64_t M, int64_t N, int64_t K, void* out, void* ws, size_t ws_bytes,
+                     int32_t* dev_err, kvc_stream_t stream) {
   if (M < 0 || N <= 0 || K <= 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
       K >= (int64_t(1) << 31))
     return KVC_EINVAL;
@@ -534,9 +534,11 @@ int32_t kvc_gemm_fp4(const uint8_t* a_codes, const uint8_t* a_scales, const floa
       !aligned16(out) || (reinterpret_cast<uintptr_t>(a_gscale) & 3u) ||
       (reinterpret_cast<uintptr_t>(b_gscale) & 3u) || (reinterpret_cast<uintptr_t>(dev_err) & 3u))
     return KVC_EINVAL;
-  if (N % 256 != 0 || K % 256 != 0) return KVC_EUNSUPPORTED;
-  if (((M + 127) / 128) * (N / 256) >= (int64_t(1) << 31)) return KVC_EUNSUPPORTED;
-  GemmFp4Launch g{a_codes, a_scales, a_gscale, b_codes, b_scales, b_gscale, M, N, K, out, dev_err};
+  if (N % 32 != 0 || K % 256 != 0) return KVC_EUNSUPPORTED;
+  if (((M + 127) / 128) * ((N + 191) / 192) >= (int64_t(1) << 31)) return KVC_EUNSUPPORTED;
+  if (ws && (!aligned16(ws) || (uint64_t)ws_bytes < (uint64_t)gemm_fp4_ws_bytes(M, N, K)))
+    return KVC_EINVAL;
+  GemmFp4Launch g{a_codes, a_scales, a_gscale, b_codes, b_scales, b_gscale, M, N, K, out, dev_err, ws};
   return cuda_status(launch_gemm_fp4(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -133,19 +133,24 @@ def test_quant_and_watchdog_validation(lib):
     # launch; M = 0 returns at once
     g = ctypes.c_void_p(0x10000004)
     ok = (x, x, g, x, x, g)
-    assert lib.kvc_gemm_fp4(*ok, 0, 256, 256, x, None, None) == _abi.KVC_OK
-    assert lib.kvc_gemm_fp4(None, None, None, None, None, None, 0, 256, 256, None, None,
-                            None) == _abi.KVC_OK
-    assert lib.kvc_gemm_fp4(None, x, g, x, x, g, 4, 256, 256, x, None, None) == _abi.KVC_EINVAL
-    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, None, None, None) == _abi.KVC_EINVAL
-    assert lib.kvc_gemm_fp4(*ok, -1, 256, 256, x, None, None) == _abi.KVC_EINVAL
-    assert lib.kvc_gemm_fp4(*ok, 4, 0, 256, x, None, None) == _abi.KVC_EINVAL
-    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, ctypes.c_void_p(0x10000008), None,
+    assert lib.kvc_gemm_fp4(*ok, 0, 256, 256, x, None, 0, None, None) == _abi.KVC_OK
+    assert lib.kvc_gemm_fp4(None, None, None, None, None, None, 0, 256, 256, None, None, 0,
+                            None, None) == _abi.KVC_OK
+    assert lib.kvc_gemm_fp4(None, x, g, x, x, g, 4, 256, 256, x, None, 0, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, None, None, 0, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, -1, 256, 256, x, None, 0, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 0, 256, x, None, 0, None, None) == _abi.KVC_EINVAL
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, ctypes.c_void_p(0x10000008), None, 0, None,
                             None) == _abi.KVC_EINVAL                   # out not 16-byte aligned
-    assert lib.kvc_gemm_fp4(x, x, ctypes.c_void_p(0x10000002), x, x, g, 4, 256, 256, x, None,
-                            None) == _abi.KVC_EINVAL                   # gscale not 4-byte aligned
-    assert lib.kvc_gemm_fp4(*ok, 4, 128, 256, x, None, None) == _abi.KVC_EUNSUPPORTED
-    assert lib.kvc_gemm_fp4(*ok, 4, 256, 128, x, None, None) == _abi.KVC_EUNSUPPORTED
+    assert lib.kvc_gemm_fp4(x, x, ctypes.c_void_p(0x10000002), x, x, g, 4, 256, 256, x, None, 0,
+                            None, None) == _abi.KVC_EINVAL             # gscale not 4-byte aligned
+    need = (4 + 256) * 256 * 2
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, x, x, need - 1, None,
+                            None) == _abi.KVC_EINVAL                   # workspace too small
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 256, x, ctypes.c_void_p(0x10000008), need, None,
+                            None) == _abi.KVC_EINVAL                   # workspace misaligned
+    assert lib.kvc_gemm_fp4(*ok, 4, 100, 256, x, None, 0, None, None) == _abi.KVC_EUNSUPPORTED
+    assert lib.kvc_gemm_fp4(*ok, 4, 256, 128, x, None, 0, None, None) == _abi.KVC_EUNSUPPORTED
     assert lib.kvc_watchdog_selftest(None, 10, None) == _abi.KVC_EINVAL
     assert lib.kvc_watchdog_selftest(x, 0, None) == _abi.KVC_EINVAL
     assert lib.kvc_status_string(_abi.KVC_ESTATE).decode().startswith("invalid in")

@@ -53,33 +53,42 @@ def _check(got: np.ndarray, a, b, rows=None, what=""):
     return want
 
 
-def _run(swl, a_dev, b_dev, M, N, K):
+def _run(swl, a_dev, b_dev, M, N, K, two_phase=False):
+    """The kernel's output as float64; two_phase: through a workspace
+    (decode once, then the f16 GEMM) filled with garbage first."""
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    swl.gemm_fp4(a_dev, b_dev, M, N, K, out=out, dev_err=err)
+    ws = None
+    if two_phase:
+        ws = torch.full((swl.gemm_fp4_ws_bytes(M, N, K),), 0xFF, dtype=torch.uint8, device="cuda")
+    swl.gemm_fp4(a_dev, b_dev, M, N, K, out=out, ws=ws, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, "a kernel wait ran out"
     return out.float().cpu().numpy().astype(np.float64)
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (1, 256, 256),        # one row, one tile
-    (128, 256, 256),      # exactly one tile
-    (300, 512, 512),      # ragged last row tile, 2 column tiles, 2 raw stages
-    (129, 768, 1024),     # one row past a tile, 3 column tiles, 4 raw stages
-    (1000, 1536, 768),    # 8 x 6 tiles, ragged tail
-    (2500, 4096, 256),    # 20 x 16 tiles: more than two per CTA (both accumulators reused)
+    (1, 192, 256),        # one row, one tile
+    (128, 192, 256),      # exactly one tile
+    (300, 384, 512),      # ragged last row tile, 2 column tiles, 2 raw stages
+    (129, 768, 1024),     # one row past a tile, 4 column tiles, 4 raw stages
+    (200, 32, 256),       # one 32-column chunk of a column tile
+    (250, 544, 512),      # ragged last column tile (544 = 2 x 192 + 160)
+    (1000, 1536, 768),    # 8 x 8 tiles, ragged row tail
+    (2500, 4096, 256),    # 20 x 22 tiles (the last ragged): several per CTA
 ])
-def test_gemm_fp4_small_shapes(swl, M, N, K):
+@pytest.mark.parametrize("two_phase", [False, True], ids=["fused", "two_phase"])
+def test_gemm_fp4_small_shapes(swl, M, N, K, two_phase):
     x = gaussian_bf16((M, K), 1.0, 91, M, N, K).float().numpy()
     w = gaussian_outliers_bf16((N, K), 0.01, 8.0, 92, M, N, K).float().numpy() * 0.02
     a, a_dev = _encode(x)
     b, b_dev = _encode(w)
-    got = _run(swl, a_dev, b_dev, M, N, K)
+    got = _run(swl, a_dev, b_dev, M, N, K, two_phase)
     _check(got, a, b, what=f"{M}x{N}x{K}")
 
 
-def test_gemm_fp4_exact_on_grid(swl):
+@pytest.mark.parametrize("two_phase", [False, True], ids=["fused", "two_phase"])
+def test_gemm_fp4_exact_on_grid(swl, two_phase):
     """Operands already on the FP4 grid: E2M1 values, every block maximum 6,
     and row 0's first block times 1.75 (maximum 10.5 = 2688 / 2^8, so the
     tensor scale is 2^-8 and every block scale, 256 or 448, is exact).  Every
@@ -101,7 +110,7 @@ def test_gemm_fp4_exact_on_grid(swl):
     b, b_dev = _encode(w)
     assert float(a[2]) == 2.0 ** -8 and float(b[2]) == 2.0 ** -8
     assert np.array_equal(ofp4.dequantize(*a), x) and np.array_equal(ofp4.dequantize(*b), w)
-    got = _run(swl, a_dev, b_dev, M, N, K)
+    got = _run(swl, a_dev, b_dev, M, N, K, two_phase)
     want = x @ w.T
     assert np.all(np.abs(x) @ np.abs(w).T < 2.0 ** 17)
     assert np.array_equal(want.astype(np.float32).astype(np.float64), want)
@@ -109,7 +118,8 @@ def test_gemm_fp4_exact_on_grid(swl):
     assert np.array_equal(got, want_bf16)
 
 
-def test_gemm_fp4_layer_projection_full_size(swl):
+@pytest.mark.parametrize("two_phase", [False, True], ids=["fused", "two_phase"])
+def test_gemm_fp4_layer_projection_full_size(swl, two_phase):
     """One LongLive-1.3B chunk's Q|K|V projection (4680 tokens x 1536 ->
     4608) in W4A4, every column of 66 sampled rows (every 73rd and the last)."""
     sh = LAYER_1P3B
@@ -118,7 +128,7 @@ def test_gemm_fp4_layer_projection_full_size(swl):
     N = w.shape[1]
     a, a_dev = _encode(hid.float().numpy())
     b, b_dev = _encode(np.ascontiguousarray(w.float().numpy().T))
-    got = _run(swl, a_dev, b_dev, M, N, K)
+    got = _run(swl, a_dev, b_dev, M, N, K, two_phase)
     assert np.isfinite(got).all()
     rows = np.unique(np.concatenate([np.arange(0, M, 73), [M - 1]]))
     _check(got, a, b, rows=rows, what="layer Q|K|V projection")
@@ -130,15 +140,17 @@ def test_gemm_fp4_zero_and_empty(swl):
     M, N, K = 130, 256, 256
     a, a_dev = _encode(np.zeros((M, K), np.float32))
     b, b_dev = _encode(gaussian_bf16((N, K), 1.0, 93).float().numpy())
-    got = _run(swl, a_dev, b_dev, M, N, K)
-    assert np.array_equal(got, np.zeros((M, N)))
+    for two_phase in (False, True):
+        got = _run(swl, a_dev, b_dev, M, N, K, two_phase)
+        assert np.array_equal(got, np.zeros((M, N)))
     out = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
     e = (a_dev[0][:0], a_dev[1][:0], a_dev[2])
     swl.gemm_fp4(e, b_dev, 0, N, K, out=out)
     torch.cuda.synchronize()
 
 
-def test_gemm_fp4_magnitude_extremes(swl):
+@pytest.mark.parametrize("two_phase", [False, True], ids=["fused", "two_phase"])
+def test_gemm_fp4_magnitude_extremes(swl, two_phase):
     """Block maxima from 2^-30 to 2^12 within one tensor (block scales over
     E4M3's whole range, subnormal ones included) and a weight at the format's
     top (decoded values up to 2688 before the tensor scale)."""
@@ -149,12 +161,16 @@ def test_gemm_fp4_magnitude_extremes(swl):
     w = rng.standard_normal((N, K)).astype(np.float32) * 1e4
     a, a_dev = _encode(x)
     b, b_dev = _encode(w)
-    got = _run(swl, a_dev, b_dev, M, N, K)
+    got = _run(swl, a_dev, b_dev, M, N, K, two_phase)
     _check(got, a, b, what="extremes")
 
 
 def test_gemm_fp4_rejects_unsupported(swl):
     a, a_dev = _encode(np.ones((4, 256), np.float32))
-    b, b_dev = _encode(np.ones((128, 256), np.float32))
+    b, b_dev = _encode(np.ones((112, 256), np.float32))
     with pytest.raises(swl.KvcError):
-        swl.gemm_fp4(a_dev, b_dev, 4, 128, 256)  # N % 256 != 0
+        swl.gemm_fp4(a_dev, b_dev, 4, 112, 256)  # N % 32 != 0
+    b, b_dev = _encode(np.ones((128, 256), np.float32))
+    short = torch.empty(swl.gemm_fp4_ws_bytes(4, 128, 256) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(swl.KvcError):
+        swl.gemm_fp4(a_dev, b_dev, 4, 128, 256, ws=short)  # workspace too small
