@@ -218,13 +218,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
           cbase[i] = (tk[i].is_a ? sm.a_codes[s] : sm.b_codes[s]) + r * 128;
         }
         const int sw = lane & 7;  // (row & 7): the rows of a task start at multiples of 32
+        // 16-byte chunk 2 j + half of the raw row: the next stage's chunk is
+        // loaded before this stage's decode, so the load latency overlaps it
+        uint4 nxt[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          nxt[i] = *reinterpret_cast<const uint4*>(cbase[i] + ((tk[i].half ^ sw) << 4));
 #pragma unroll 1
         for (int j = 0; j < GKR / GKD; ++j, ++ds) {
           const int d = ds % kDecStages;
           uint4 codes[2];
 #pragma unroll
-          for (int i = 0; i < 2; ++i)  // 16-byte chunk 2 j + half of the raw row
-            codes[i] = *reinterpret_cast<const uint4*>(cbase[i] + (((2 * j + tk[i].half) ^ sw) << 4));
+          for (int i = 0; i < 2; ++i) {
+            codes[i] = nxt[i];
+            if (j + 1 < GKR / GKD)
+              nxt[i] = *reinterpret_cast<const uint4*>(cbase[i] + (((2 * (j + 1) + tk[i].half) ^ sw) << 4));
+          }
           if (ds >= kDecStages && !mbar_wait(&sm.dec_empty[d], ((ds / kDecStages) - 1) & 1, wd)) {
             ok = false;
             break;
