@@ -56,10 +56,11 @@ WORKLOAD = ("LongLive-1.3B layer chunk step: 12 heads x 128, 4680 queries/chunk,
 # ncu dram bytes per launch of the dominant kernel, with the hash of the source
 # they were taken on (null once the kernel changed)
 TRAFFIC = {
-    # ncu --set full on the LongLive-1.3B layer workload (one launch each);
-    # summary in profiles/sinkwin_attn_layer1p3b_18720keys.md
-    "sinkwin_attn_kernel<128,false>": {"bytes": 305278720 + 26565120, "src_sha": "b4ae518685bd2dfc"},
-    "sinkwin_attn_kernel<128,true>": {"bytes": 47181056 + 4062208, "src_sha": "b4ae518685bd2dfc"},
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum on the LongLive-1.3B
+    # layer workload (one launch each); summary in
+    # profiles/sinkwin_attn_layer1p3b_18720keys.md
+    "sinkwin_attn_kernel<128,false>": {"bytes": 305712896 + 26446336, "src_sha": "8c2658ee2d3f6471"},
+    "sinkwin_attn_kernel<128,true>": {"bytes": 47215872 + 1064704, "src_sha": "8c2658ee2d3f6471"},
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
     "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
