@@ -63,6 +63,10 @@ struct AttnLaunch {
   const float* k_gscale;
   const float* v_gscale;
   int32_t chunk_tokens;  // rows per region (FP4: region of a row -> its tensor scale)
+  // FP4 cache decoded beforehand: f16 [S][H][D] K and V (e2m1 * s, no tensor
+  // scale) of every visible region, or null (decoded inside the kernel)
+  const void* k16;
+  const void* v16;
   // split-item workspace (null: whole items per CTA)
   void* ws;
   size_t ws_bytes;
@@ -134,6 +138,24 @@ struct GemmFp4Launch {
   void* ws;                 // null: fused kernel; else gemm_fp4_ws_bytes(M, N, K) bytes
 };
 cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st);
+// FP4 -> f16 (e2m1 * e4m3 scale, exact; no tensor scale) of contiguous runs:
+// codes [groups * 4] bytes, scales [groups / 2], out [groups * 8] f16; groups
+// (of 8 elements) even, all pointers 16-byte aligned.
+struct Fp4DecodeJob {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  void* out;
+  int64_t groups;
+  int32_t g_region;  // -1: no tensor scale; else the output is rounded to f16 after
+                     // multiplying by gscale[g_region] / G (see below)
+};
+constexpr int kMaxDecodeJobs = 2 * (1 + KVC_MAX_WINDOW);
+// gscale: device tensor scales (used by jobs with g_region >= 0); G is the
+// power of two of the FP4 attention's V shift: from the largest of
+// gscale[regions[0..nregions)], as the attention kernel computes it.
+cudaError_t launch_fp4_to_f16(const Fp4DecodeJob* jobs, int njobs, cudaStream_t st,
+                              const float* gscale = nullptr, const int32_t* regions = nullptr,
+                              int nregions = 0);
 size_t gemm_fp4_smem_bytes();
 int64_t gemm_fp4_ws_bytes(int64_t M, int64_t N, int64_t K);
 

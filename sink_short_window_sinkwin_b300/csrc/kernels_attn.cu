@@ -349,8 +349,16 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long* a, unsign
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
 }
 
-template <int D, bool kFp4>
-__global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
+// kPre (FP4 caches only): K and V were decoded to f16 by a pass before the
+// launch (K' = e2m1 * s exactly; V' = e2m1 * s * g_V / G rounded once to f16,
+// G the V shift below).  The kernel then has the bf16 kernel's shape (no
+// decode warps, no register split): the TMA producer loads f16 K/V tiles, and
+// each softmax thread converts its own query row to f16 at the start of a
+// piece, keeping the row's scale in a register.  Otherwise the arithmetic is
+// the FP4 path's (f16 operands, K's tensor scale in the logit scale, G
+// multiplied back in the normalisation); P is stored as plain f16.
+template <int D, bool kFp4, bool kPre = false>
+__global__ void __launch_bounds__(attn_threads<kFp4 && !kPre>(), 1)
     sinkwin_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
@@ -362,11 +370,13 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = blockIdx.x;
-  const uint32_t kvfull_count = kFp4 ? 128u : 1u;
+  static_assert(kFp4 || !kPre, "pre-decoded tiles exist only for FP4 caches");
+  constexpr bool kTmaKV = !kFp4 || kPre;  // K/V tiles arrive by TMA
+  const uint32_t kvfull_count = kTmaKV ? 1u : 128u;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.bar_q, 1);
-    mbar_init(&sm.bar_qcvt, BN);
+    mbar_init(&sm.bar_qcvt, kPre ? 2 * BM : BN);  // converted by the softmax / decode threads
     mbar_init(&sm.bar_qread, 2 * BM);
     mbar_init(&sm.bar_qempty, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
   }
   if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
-    if (!kFp4) {
+    if (kTmaKV) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
     }
@@ -405,7 +415,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
 
   if (warp >= kTmaWarp && warp < kTmaWarp + 4) {
     // warpgroup 2: TMA producer, MMA issuer (FP4: two idle warps)
-    if constexpr (kFp4) setmaxnreg_dec<RegSplit<true>::kCtl>();
+    if constexpr (kFp4 && !kPre) setmaxnreg_dec<RegSplit<true>::kCtl>();
     if (warp == kTmaWarp) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -421,13 +431,13 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
           if (npc > 0 && !mbar_wait(&sm.bar_qempty, (npc - 1) & 1, wd)) break;
           // FP4: the next Q (and its row scales) only once the softmax threads
           // hold the previous piece's scales
-          if (kFp4 && npc > 0 && !mbar_wait(&sm.bar_qread, (npc - 1) & 1, wd)) break;
+          if (kFp4 && !kPre && npc > 0 && !mbar_wait(&sm.bar_qread, (npc - 1) & 1, wd)) break;
           mbar_expect_tx(&sm.bar_q, (act1 ? 2u : 1u) * DB * BM * 64 * 2);
           for (int s = 0; s < (act1 ? 2 : 1); ++s)
             for (int db = 0; db < DB; ++db)
               tma_load_3d(&sm.q[s][db][0], &tmQ, &sm.bar_q, db * 64, h, m0 + s * BM);
           ++npc;
-          if (!kFp4) {
+          if (kTmaKV) {
             KvCursor cur;
             cur.seek(p, Share::first_tile(p, pc));
             const uint32_t tbytes = DB * BN * 64 * 2;
@@ -587,8 +597,8 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
         mbar_drain(&sm.bar_drain, 0);
       }
     }
-  } else if (kFp4 && warp >= kDequantWarp0) {
-    if constexpr (kFp4) setmaxnreg_dec<RegSplit<true>::kDecode>();
+  } else if (kFp4 && !kPre && warp >= kDequantWarp0) {
+    if constexpr (kFp4 && !kPre) setmaxnreg_dec<RegSplit<true>::kDecode>();
     // ------------------------------------------------------------ FP4 dequant producer
     const int r = threadIdx.x - kDequantWarp0 * 32;  // key row within the tile
     RawRing<D>& raw = *reinterpret_cast<RawRing<D>*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(Smem));
@@ -675,7 +685,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
     }
     cp_async_wait<0>();  // no copy into this CTA's shared memory outlives it
   } else if (warp < kSoftmaxWarps) {
-    if constexpr (kFp4) setmaxnreg_inc<RegSplit<true>::kSoftmax>();
+    if constexpr (kFp4 && !kPre) setmaxnreg_inc<RegSplit<true>::kSoftmax>();
     // ------------------------------------------------------------ softmax
     const int slot = warp >> 2;
     const int wq = warp & 3;
@@ -715,7 +725,20 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
       const uint32_t it0 = it;
       it += n;
       [[maybe_unused]] float qinv = 1.0f;
-      if constexpr (kFp4) {
+      if constexpr (kPre) {
+        // this thread's query row of its slot, once the piece's Q landed: to
+        // f16 in place with its power-of-two scale (both slots arrive, so the
+        // count holds when slot 1 is idle)
+        const bool got = mbar_wait(&sm.bar_q, nq & 1, wd);
+        ++nq;
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (slot == 0 || act1) convert_q_row<D>(sm.q[slot], row, &qinv);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_qcvt);
+      } else if constexpr (kFp4) {
         // every piece converts Q once (both slots' rows in the same phase)
         const bool got = mbar_wait(&sm.bar_qcvt, nq & 1, wd);
         ++nq;
@@ -768,7 +791,7 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
         ++ns;
         tc_fence_after();
         const int valid = cur.valid(p);
-        if (!kFp4 && slot == 0 && valid < BN) {
+        if (kTmaKV && slot == 0 && valid < BN) {
           // key rows past the segment end may hold anything (NaN scrub,
           // never-written memory): zero them in the V stage before P*V
           const uint32_t ti = it0 + i;
@@ -838,7 +861,9 @@ __global__ void __launch_bounds__(attn_threads<kFp4>(), 1)
             const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
             const uint64_t p2 = f32x2(p0, p1);
             acc2 = fadd2(acc2, p2);
-            if constexpr (kFp4) {
+            if constexpr (kPre) {
+              pk[e] = pack_f16x2(p0, p1);  // the V tensor scale is in the decoded V
+            } else if constexpr (kFp4) {
               float q0, q1;
               f32x2_split(fmul2(p2, g2), q0, q1);
               pk[e] = pack_f16x2(q0, q1);
@@ -991,16 +1016,20 @@ int sm_count() {
   return cache[dev];
 }
 
-template <int D, bool kFp4>
+template <int D, bool kFp4, bool kPre = false>
 cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   CUtensorMap tq{}, tk{}, tv{};
   const uint64_t rs = (uint64_t)a.H * a.D * 2;  // bytes per token row
   if (!encode_tmap_3d_bf16(&tq, a.q, a.D, a.H, a.tq, (uint64_t)a.D * 2, rs, 64, 1, BM, true))
     return cudaErrorInvalidValue;
-  if (!kFp4) {
-    if (!encode_tmap_3d_bf16(&tk, a.k, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
+  if (!kFp4 || kPre) {
+    // bf16 cache, or the f16 tiles of a pre-decoded FP4 cache (2-byte
+    // elements either way; the map's type only sizes them)
+    const void* kb = kPre ? a.k16 : a.k;
+    const void* vb = kPre ? a.v16 : a.v;
+    if (!encode_tmap_3d_bf16(&tk, kb, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
       return cudaErrorInvalidValue;
-    if (!encode_tmap_3d_bf16(&tv, a.v, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
+    if (!encode_tmap_3d_bf16(&tv, vb, a.D, a.H, a.S, (uint64_t)a.D * 2, rs, 64, 1, BN, true))
       return cudaErrorInvalidValue;
   } else {
     tk = tq;  // unused
@@ -1057,13 +1086,13 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   }
   // one CTA per SM: a second resident CTA would wait in tcgen05.alloc for the
   // 512 TMEM columns the first one holds
-  size_t smem = sizeof(AttnSmem<D>) + (kFp4 ? sizeof(RawRing<D>) : 0) + 1024;
+  size_t smem = sizeof(AttnSmem<D>) + (kFp4 && !kPre ? sizeof(RawRing<D>) : 0) + 1024;
   if (smem < 120 * 1024) smem = 120 * 1024;
-  auto kern = sinkwin_attn_kernel<D, kFp4>;
+  auto kern = sinkwin_attn_kernel<D, kFp4, kPre>;
   static bool smem_set[64] = {};  // one per instantiation of this launcher
   cudaError_t e = set_smem_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
-  if constexpr (kFp4) {
+  if constexpr (kFp4 && !kPre) {
     // the setmaxnreg split hands out exactly the registers the block launches
     // with: refuse to launch if the compiled kernel's count differs (an
     // increase that the launch cannot cover would wait forever)
@@ -1080,7 +1109,7 @@ cudaError_t launch_attn_t(const AttnLaunch& a, cudaStream_t st) {
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.G, 1, 1);
-  cfg.blockDim = dim3(attn_threads<kFp4>(), 1, 1);
+  cfg.blockDim = dim3(attn_threads<kFp4 && !kPre>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   // a merge waits on a neighbouring CTA: all CTAs must be resident together
@@ -1101,8 +1130,13 @@ size_t attn_workspace_bytes(int D, int ctas) {
 int attn_sm_count() { return sm_count(); }
 
 cudaError_t launch_sinkwin_attn(const AttnLaunch& a, cudaStream_t st) {
-  if (a.D == 128) return a.fp4 ? launch_attn_t<128, true>(a, st) : launch_attn_t<128, false>(a, st);
-  if (a.D == 64) return a.fp4 ? launch_attn_t<64, true>(a, st) : launch_attn_t<64, false>(a, st);
+  const bool pre = a.fp4 && a.k16 && a.v16;
+  if (a.D == 128)
+    return !a.fp4 ? launch_attn_t<128, false>(a, st)
+                  : (pre ? launch_attn_t<128, true, true>(a, st) : launch_attn_t<128, true>(a, st));
+  if (a.D == 64)
+    return !a.fp4 ? launch_attn_t<64, false>(a, st)
+                  : (pre ? launch_attn_t<64, true, true>(a, st) : launch_attn_t<64, true>(a, st));
   return cudaErrorInvalidValue;
 }
 

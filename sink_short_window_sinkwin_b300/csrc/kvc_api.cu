@@ -393,7 +393,35 @@ int32_t sinkwin_attn(const kvc_cache* c, const void* q, void* out, int32_t tq, f
   a.chunk_tokens = Tc;
   a.ws = c->attn_ws;
   a.ws_bytes = c->attn_ws ? (size_t)c->attn_ws_bytes : 0;
-  return cuda_status(launch_sinkwin_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // FP4 cache with room in the staging buffer for f16 K and V of every region:
+  // decode the visible regions once, then the attention loads f16 tiles by TMA
+  // instead of decoding each tile for every query item.  K' = e2m1 * s (exact;
+  // its tensor scale joins the logit scale), V' = f16(e2m1 * s * g_V / G) with
+  // G the kernel's power-of-two V shift (so P needs no per-element factor)
+  const size_t kv16 = (size_t)a.S * a.H * a.D * 2;  // bytes of one f16 K (or V)
+  if (a.fp4 && stage_ok(c, 2 * kv16)) {
+    uint8_t* k16 = static_cast<uint8_t*>(c->stage);
+    uint8_t* v16 = k16 + kv16;
+    Fp4DecodeJob jobs[kMaxDecodeJobs];
+    int32_t regions[1 + KVC_MAX_WINDOW];
+    int nj = 0;
+    const size_t row_elems = (size_t)a.H * a.D;
+    for (int i = 0; i < a.nseg; ++i) {
+      const size_t e0 = (size_t)a.seg[i].row0 * row_elems, ne = (size_t)a.seg[i].rows * row_elems;
+      const int32_t region = a.seg[i].row0 / Tc;
+      regions[i] = region;
+      const uint8_t* kc = static_cast<const uint8_t*>(c->k);
+      const uint8_t* vc = static_cast<const uint8_t*>(c->v);
+      jobs[nj++] = Fp4DecodeJob{kc + e0 / 2, c->k_scale + e0 / 16, k16 + e0 * 2, (int64_t)(ne / 8), -1};
+      jobs[nj++] = Fp4DecodeJob{vc + e0 / 2, c->v_scale + e0 / 16, v16 + e0 * 2, (int64_t)(ne / 8), region};
+    }
+    const cudaError_t e = launch_fp4_to_f16(jobs, nj, st, c->v_gscale, regions, a.nseg);
+    if (e != cudaSuccess) return cuda_status(e);
+    a.k16 = k16;
+    a.v16 = v16;
+  }
+  return cuda_status(launch_sinkwin_attn(a, st));
 }
 
 int32_t kvc_recache(kvc_cache* c, const void* hidden, const void* w_kv, const float* gamma_k,

@@ -109,9 +109,14 @@ def test_quant_bitexact_near_scale_midpoints(swl):
         _check_quant(swl, x, f"near-midpoint blocks, tensor amax {amax_t:g} ({len(maxima)} blocks)")
 
 
-def _fp4_stream(swl, sh, cfg, steps, dist):
+# FP4 attention runs two ways: K/V decoded inside the kernel (no staging
+# buffer) or decoded beforehand into the staging buffer and loaded by TMA
+PRE = pytest.mark.parametrize("stage", [False, True], ids=["in_kernel", "predecoded"])
+
+
+def _fp4_stream(swl, sh, cfg, steps, dist, stage=False):
     cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
-                        sh.window_chunks, dtype="fp4")
+                        sh.window_chunks, dtype="fp4", stage=stage)
     model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
     W, Tc = sh.window_chunks, sh.chunk_tokens
     enc = {}
@@ -137,10 +142,11 @@ def _fp4_stream(swl, sh, cfg, steps, dist):
         yield c, q, cache, model
 
 
-def test_fp4_tiny_stream(swl):
+@PRE
+def test_fp4_tiny_stream(swl, stage):
     sh = TINY
     scale = 1.0 / math.sqrt(sh.head_dim)
-    for c, q, cache, model in _fp4_stream(swl, sh, 0, 6, "outliers"):
+    for c, q, cache, model in _fp4_stream(swl, sh, 0, 6, "outliers", stage):
         out = cache.attn(q.cuda(), scale)
         torch.cuda.synchronize()
         want = oatt.sinkwin_attention(model, bf16_to_f64(q), scale)
@@ -148,11 +154,12 @@ def test_fp4_tiny_stream(swl):
                  plus_output_rounding=True)
 
 
+@PRE
 @pytest.mark.parametrize("H,D,tpf,cf,W,tq", [(2, 128, 100, 1, 3, 130), (3, 64, 50, 3, 2, 300)])
-def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
+def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq, stage):
     sh = Shapes(H, D, tpf, cf, W, 1, tpf)
     scale = 1.0 / math.sqrt(D)
-    for c, q, cache, model in _fp4_stream(swl, sh, 5, W + 2, "outliers"):
+    for c, q, cache, model in _fp4_stream(swl, sh, 5, W + 2, "outliers", stage):
         qq = chunk_qkv(sh, 6, 0, c, "rms1", q_rows=tq)[0]
         out = cache.attn(qq.cuda(), scale)
         torch.cuda.synchronize()
@@ -161,8 +168,9 @@ def test_fp4_small_shapes(swl, H, D, tpf, cf, W, tq):
                  plus_output_rounding=True)
 
 
+@PRE
 @pytest.mark.parametrize("where", ["every_tile", "late_tile"])
-def test_fp4_max_jump_within_tile(swl, where):
+def test_fp4_max_jump_within_tile(swl, where, stage):
     """Keys 64..127 of a 128-key tile whose logits lie more than 2^8 (log2
     units) above those of keys 0..63 and of the tiles before: the softmax must
     move its held reference maximum (and rescale O) before forming that tile's
@@ -174,7 +182,7 @@ def test_fp4_max_jump_within_tile(swl, where):
     rng = np.random.default_rng(31)
     u = rng.standard_normal(D)
     u /= np.linalg.norm(u)
-    cache = swl.KVCache(H, D, 128, 2, W, dtype="fp4")
+    cache = swl.KVCache(H, D, 128, 2, W, dtype="fp4", stage=stage)
     model = CacheModel(H, D, Tc, W)
     for c in range(1 + W):
         k = rng.standard_normal((Tc, H, D)) * 0.3
@@ -198,8 +206,9 @@ def test_fp4_max_jump_within_tile(swl, where):
     assert cache.last_device_error() == swl.KVC_OK
 
 
+@PRE
 @pytest.mark.parametrize("vmag", [2.0 ** -14, 2.0 ** 26])
-def test_fp4_v_magnitude_extremes(swl, vmag):
+def test_fp4_v_magnitude_extremes(swl, vmag, stage):
     """P is stored as f16 times the V tensor scale g_V (up to 2^8 under a held
     running max).  V of magnitude 2^-14 (g_V ~ 1e-7: f16 subnormal products) or
     2^26 (g_V ~ 1e5: beyond the f16 range) must give the oracle's output scaled
@@ -208,7 +217,7 @@ def test_fp4_v_magnitude_extremes(swl, vmag):
     of two, exact)."""
     H, D, W = 2, 128, 2
     rng = np.random.default_rng(41)
-    cache = swl.KVCache(H, D, 128, 1, W, dtype="fp4")
+    cache = swl.KVCache(H, D, 128, 1, W, dtype="fp4", stage=stage)
     model = CacheModel(H, D, 128, W)
     for c in range(1 + W):
         k = rng.standard_normal((128, H, D))
@@ -228,10 +237,11 @@ def test_fp4_v_magnitude_extremes(swl, vmag):
     assert cache.last_device_error() == swl.KVC_OK
 
 
-def test_fp4_layer_full_size(swl):
+@PRE
+def test_fp4_layer_full_size(swl, stage):
     sh = LAYER_1P3B
     scale = 1.0 / math.sqrt(sh.head_dim)
-    *_, (c, q, cache, model) = list(_fp4_stream(swl, sh, 3, 4, "outliers"))
+    *_, (c, q, cache, model) = list(_fp4_stream(swl, sh, 3, 4, "outliers", stage))
     out = cache.attn(q.cuda(), scale)
     torch.cuda.synchronize()
     kk, vv = model.visible_kv()
@@ -241,12 +251,13 @@ def test_fp4_layer_full_size(swl):
     assert cache.last_device_error() == swl.KVC_OK
 
 
-def test_fp4_many_items_full_compare(swl):
+@PRE
+def test_fp4_many_items_full_compare(swl, stage):
     """FP4 cache, 228 items on 148 CTAs (step-balanced shares, merged pieces),
     one segment per region, full compare of all 4680 x 12 rows."""
     sh = Shapes(12, 128, 100, 1, 2, 10, 10)
     scale = 1.0 / math.sqrt(128)
-    for c, q, cache, model in _fp4_stream(swl, sh, 14, 4, "outliers"):
+    for c, q, cache, model in _fp4_stream(swl, sh, 14, 4, "outliers", stage):
         if c in (0, 3):
             qq = chunk_qkv(sh, 15, 0, c, "rms1", q_rows=4680)[0]
             out = cache.attn(qq.cuda(), scale)
@@ -257,7 +268,8 @@ def test_fp4_many_items_full_compare(swl):
     assert cache.last_device_error() == swl.KVC_OK
 
 
-def test_fp4_scrub_unaligned_regions(swl):
+@PRE
+def test_fp4_scrub_unaligned_regions(swl, stage):
     """H=3, D=64, 150-token chunks: a slot's scales span 1800 bytes, so slot
     boundaries are not 16-byte aligned.  The scrub on evict writes exactly the
     freed slot (codes 0, scales 0x7F), nothing around it, and attention over the
@@ -265,7 +277,7 @@ def test_fp4_scrub_unaligned_regions(swl):
     sh = Shapes(3, 64, 50, 3, 2, 1, 50)
     Tc = sh.chunk_tokens
     cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
-                        sh.window_chunks, dtype="fp4", scrub_on_evict=True)
+                        sh.window_chunks, dtype="fp4", scrub_on_evict=True, stage=stage)
     model = CacheModel(sh.heads, sh.head_dim, Tc, sh.window_chunks)
     for c in range(3):
         _, k, v = chunk_qkv(sh, 21, 0, c, "outliers")
