@@ -61,6 +61,8 @@ TRAFFIC = {
     # profiles/sinkwin_attn_layer1p3b_18720keys.md
     "sinkwin_attn_kernel<128,false>": {"bytes": 305712896 + 26446336, "src_sha": "8c2658ee2d3f6471"},
     "sinkwin_attn_kernel<128,true>": {"bytes": 47215872 + 1064704, "src_sha": "8c2658ee2d3f6471"},
+    # the FP4 attention with a staging buffer: the decode pass and the kernel,
+    # one call (the bench times the call)
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
     "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
@@ -425,11 +427,14 @@ def main():
     gamma = torch.ones(HD, dtype=torch.float32, device=dev)
     layers = []
     nlayers = max(1, args.layers)
+    # one staging buffer shared by the layers' FP4 caches (their calls are
+    # stream-ordered): the FP4 attention decodes the visible K/V into it
+    stage4 = torch.empty(4 * TC * HD * 4, dtype=torch.uint8, device=dev)
     for li in range(nlayers):
         L = {
             "bf": swl.KVCache(H, D, TPF, CF, W, dtype="bf16", device=dev,
                               stage=2 * TC * HD * 4),  # the chunk projection's fp32 Q|K rows
-            "f4": swl.KVCache(H, D, TPF, CF, W, dtype="fp4", device=dev),
+            "f4": swl.KVCache(H, D, TPF, CF, W, dtype="fp4", device=dev, stage=stage4),
             "q": randn((TC, H, D), 1 / math.sqrt(D)),
             "k": randn((TC, H, D), 1 / math.sqrt(D)),
             "v": randn((TC, H, D)),
@@ -473,8 +478,9 @@ def main():
 
     # recache (the fused cluster launch and its cluster-free side launch),
     # chunk projection (GEMM, norm+RoPE), bf16 attention, FP4 append (amax,
-    # encode), FP4 attention; evict without scrub launches nothing
-    launches_per_step = 2 + 2 + 1 + 2 + 1
+    # encode), FP4 attention (K/V decode into the staging buffer, attention);
+    # evict without scrub launches nothing
+    launches_per_step = 2 + 2 + 1 + 2 + 2
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ROWS) + 1)]
           for _ in range(args.steps)]
@@ -626,7 +632,8 @@ def main():
             d["latent_frames_per_s_per_layer"] = CF / (per[r] * 1e-3)
         rows[r] = d
     dom = max(("attn_bf16", "attn_fp4", "recache"), key=lambda r: per[r])
-    kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>", "attn_fp4": "sinkwin_attn_kernel<128,true>",
+    kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>",
+             "attn_fp4": "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>",
              "recache": "recache_fused_kernel"}[dom]
     src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_attn.cu",
            "recache": "kernels_recache.cu"}[dom]

@@ -100,10 +100,12 @@ typedef struct kvc_cache {
   uint64_t attn_ws_bytes; /* its size in bytes */
   void* stage;       /* optional staging buffer (16-byte aligned) of up to
                         kvc_cache_bytes(c, 8) bytes, or NULL: fp32 rows waiting for
-                        their RMSNorm, and bf16 K/V waiting for their FP4 encode.
+                        their RMSNorm, bf16 K/V waiting for their FP4 encode, and
+                        the f16 K/V sinkwin_attn decodes an FP4 cache into.
                         Needed by kvc_recache on an FP4 cache and by kvc_project_append
                         (each states how much it uses).  Contents need no init;
-                        calls sharing it must be stream-ordered. */
+                        calls sharing it must be stream-ordered (caches whose calls
+                        are may share one). */
   uint64_t stage_bytes; /* its size in bytes */
   /* ---- options ---- */
   int32_t scrub_on_evict;     /* nonzero: kvc_evict overwrites the freed slot with NaN */
@@ -181,10 +183,17 @@ int32_t kvc_evict(kvc_cache* c, int64_t chunk_idx, kvc_stream_t stream);
  * into 256-row items and items into pieces of K/V tiles when there are fewer
  * items than SMs (pieces merged through attn_ws; without it whole items).
  * Arithmetic: bf16 operands, fp32 accumulation and softmax, bf16 output.  FP4
- * caches are dequantised inside the tile load, exactly: K as e2m1 * s (bf16),
- * V as e2m1 * s (f16); the regions' fp32 tensor scales enter the logit scale
- * (K) and P (V, P stored as f16 after dividing every V scale by one power of
- * two covering the largest, so any finite magnitude of V is representable).
+ * caches are dequantised to f16, K as e2m1 * s (exact), and Q is converted to
+ * f16 exactly with a power-of-two scale per row; the regions' K tensor scales
+ * enter the logit scale.  Every V tensor scale is first divided by one power
+ * of two G covering the largest (G returns in the normalisation, so any
+ * finite magnitude of V is representable).  Two ways:
+ *  - stage of at least 2 * S * H * D * 2 bytes (S = (1 + W) * Tc;
+ *    kvc_cache_bytes(c, 8) is always enough): one launch decodes the visible
+ *    regions' K and V into stage, V as f16(e2m1 * s * g_V / G), then the
+ *    attention kernel loads those f16 tiles (two launches; stage overwritten);
+ *  - otherwise K/V are decoded inside the attention kernel's tile load, V as
+ *    e2m1 * s (exact), g_V / G applied to P before it is stored as f16.
  * Defined by: LongLive summary page, 方法 §3 高效长推理 (queries attend to the
  * frame-sink tokens joined with the short window); FP4 read: LongLive 2.0
  * inference blog, "NVFP4 量化与 KV Cache 压缩的工程实现" (fused dequantisation). */

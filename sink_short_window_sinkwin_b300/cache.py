@@ -47,10 +47,13 @@ class KVCache:
 
     def __init__(self, heads: int, head_dim: int, tokens_per_frame: int, chunk_frames: int,
                  window_chunks: int, dtype: str = "bf16", device="cuda", scrub_on_evict=False,
-                 attn_workspace: bool = True, stage: bool | int = False, rope_offset_frames: int = 0):
-        """stage: False (none), True (the largest any call needs, kvc_cache_bytes(c, 8)) or a
-        size in bytes -- the staging buffer kvc_recache on an FP4 cache and
-        kvc_project_append use.  rope_offset_frames: the multi-shot RoPE offset."""
+                 attn_workspace: bool = True, stage=False, rope_offset_frames: int = 0):
+        """stage: False (none), True (the largest any call needs, kvc_cache_bytes(c, 8)), a
+        size in bytes, or a contiguous CUDA tensor on the cache's device to use as the
+        buffer (several caches whose calls are stream-ordered may share one) -- the
+        staging buffer kvc_recache on an FP4 cache and kvc_project_append use, and
+        that sinkwin_attn on an FP4 cache decodes K/V into when it holds them.
+        rope_offset_frames: the multi-shot RoPE offset."""
         self.c = KvcCache()
         c = self.c
         c.heads, c.head_dim = heads, head_dim
@@ -87,8 +90,14 @@ class KVCache:
                         if attn_workspace and nbytes[7] > 0 else None)
         c.attn_ws = 0 if self.attn_ws is None else self.attn_ws.data_ptr()
         c.attn_ws_bytes = 0 if self.attn_ws is None else nbytes[7]
-        sb = nbytes[8] if stage is True else int(stage or 0)
-        self.stage = torch.empty(sb, dtype=torch.uint8, device=self.device) if sb > 0 else None
+        if isinstance(stage, torch.Tensor):
+            if not stage.is_cuda or not stage.is_contiguous() or stage.device != self.device:
+                raise ValueError("stage: expected a contiguous CUDA tensor on the cache's device")
+            self.stage = stage
+            sb = stage.numel() * stage.element_size()
+        else:
+            sb = nbytes[8] if stage is True else int(stage or 0)
+            self.stage = torch.empty(sb, dtype=torch.uint8, device=self.device) if sb > 0 else None
         c.stage = 0 if self.stage is None else self.stage.data_ptr()
         c.stage_bytes = sb
         for name, t, nb in (("k", self.k, nbytes[0]), ("v", self.v, nbytes[1]),
