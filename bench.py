@@ -59,10 +59,11 @@ TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum on the LongLive-1.3B
     # layer workload (one launch each); summary in
     # profiles/sinkwin_attn_layer1p3b_18720keys.md
-    "sinkwin_attn_kernel<128,false>": {"bytes": 305712896 + 26446336, "src_sha": "8c2658ee2d3f6471"},
-    "sinkwin_attn_kernel<128,true>": {"bytes": 47215872 + 1064704, "src_sha": "8c2658ee2d3f6471"},
-    # the FP4 attention with a staging buffer: the decode pass and the kernel,
-    # one call (the bench times the call)
+    "sinkwin_attn_kernel<128,false>": {"bytes": 310526976 + 26393344, "src_sha": "c76cdafbd9a1ff12"},
+    # the FP4 attention with a staging buffer, one call: the decode pass and
+    # the kernel (the bench times the call)
+    "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>": {
+        "bytes": (32370688 + 52944896) + (314591232 + 26115328), "src_sha": "305a49bcf1322827"},
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
     "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
@@ -80,10 +81,13 @@ def _peaks():
         return 1800.0, 1400.0, 6400.0, "fallback"
 
 
-def _src_sha(name):
-    p = os.path.join(ROOT, "sink_short_window_sinkwin_b300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _src_sha(names):
+    """Hash of the kernel sources (one file name, or several joined by '+')."""
+    h = hashlib.sha256()
+    for name in names.split("+"):
+        with open(os.path.join(ROOT, "sink_short_window_sinkwin_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ---------------------------------------------------------------------------
@@ -635,7 +639,7 @@ def main():
     kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>",
              "attn_fp4": "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>",
              "recache": "recache_fused_kernel"}[dom]
-    src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_attn.cu",
+    src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_gemm_fp4.cu+kernels_attn.cu",
            "recache": "kernels_recache.cu"}[dom]
     tr = TRAFFIC.get(kname)
     traffic = tr["bytes"] if tr and tr["src_sha"] == _src_sha(src) else None
