@@ -301,3 +301,35 @@ def test_fp4_scrub_unaligned_regions(swl, stage):
     want = oatt.sinkwin_attention(model, bf16_to_f64(q), 1.0 / math.sqrt(64))
     assert_close(to64(out), want, ATOL_FP4, None, "fp4 after unaligned scrub", plus_output_rounding=True)
     assert cache.last_device_error() == swl.KVC_OK
+
+
+def test_fp4_caches_sharing_one_staging_buffer(swl):
+    """Two FP4 caches (different contents) handed the same staging tensor: the
+    decode-once path overwrites it on every call, so calls alternating
+    between the caches must each see only their own K/V."""
+    sh = Shapes(2, 128, 100, 1, 2, 10, 10)
+    scale = 1.0 / math.sqrt(128)
+    probe = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                        sh.window_chunks, dtype="fp4", stage=True)
+    shared = probe.stage
+    caches, models = [], []
+    for cfg in (51, 52):
+        cache = swl.KVCache(sh.heads, sh.head_dim, sh.tokens_per_frame, sh.chunk_frames,
+                            sh.window_chunks, dtype="fp4", stage=shared)
+        model = CacheModel(sh.heads, sh.head_dim, sh.chunk_tokens, sh.window_chunks)
+        for c in range(1 + sh.window_chunks):
+            _, k, v = chunk_qkv(sh, cfg, 0, c, "outliers")
+            cache.append(k.cuda(), v.cuda(), c)
+            model.append(c, ofp4.dequantize(*ofp4.quantize(_f32(k))), ofp4.dequantize(*ofp4.quantize(_f32(v))))
+        caches.append(cache)
+        models.append(model)
+    for rep in range(2):
+        for i in (0, 1):
+            q = chunk_qkv(sh, 53 + i, 0, rep, "rms1", q_rows=300)[0]
+            out = caches[i].attn(q.cuda(), scale)
+            torch.cuda.synchronize()
+            want = oatt.sinkwin_attention(models[i], bf16_to_f64(q), scale)
+            assert_close(to64(out), want, ATOL_FP4, None, f"shared stage, cache {i}, round {rep}",
+                         plus_output_rounding=True)
+    for cache in caches:
+        assert cache.last_device_error() == swl.KVC_OK
