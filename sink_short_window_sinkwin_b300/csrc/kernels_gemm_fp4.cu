@@ -21,12 +21,12 @@
 // decoded A tile goes to TMEM (tcgen05.st; the MMA takes A from TMEM) and
 // only B's decoded tile is written to and read from shared memory.
 //
-// Warp roles (512 threads, one CTA per SM, persistent over 128 x 192 tiles):
-//   warps 0-9   decode: raw FP4 stage (K = 256) -> four f16 stages (K = 64):
+// Warp roles (576 threads, one CTA per SM, persistent over 128 x 192 tiles):
+//   warps 0-11  decode: raw FP4 stage (K = 256) -> four f16 stages (K = 64):
 //               A rows into TMEM, B rows into 128-byte swizzled shared memory
-//   warp 10     TMA: raw codes (128-byte swizzled) and scales of A and B
-//   warp 11     MMA issue (one thread): 4 x (128 x 192 x 16) per f16 stage
-//   warps 12-15 epilogue: TMEM -> x (g_a g_b) -> bf16 -> global
+//   warp 12     TMA: raw codes (128-byte swizzled) and scales of A and B
+//   warp 13     MMA issue (one thread): 4 x (128 x 192 x 16) per f16 stage
+//   warps 14-17 epilogue: TMEM -> x (g_a g_b) -> bf16 -> global
 // TMEM: two 192-column accumulators (columns 0-383) and two A stages of 32
 // columns (384-447).  The epilogue writes bf16 boxes of 32 x 32 through
 // shared memory with bulk tensor stores.  Every wait is bounded (the device error word records a
@@ -46,19 +46,20 @@ constexpr int GKR = 256;  // K elements per raw stage
 constexpr int GKD = 64;   // K elements per decoded f16 stage (128 bytes a row)
 constexpr int kRawStages = 3;
 constexpr int kDecStages = 2;
-constexpr int kDecodeWarps = 10;
-constexpr int kTmaWarp = 10, kMmaWarp = 11;  // warps 12-15: epilogue
-constexpr int kGThreads = 32 * 16;
+constexpr int kDecodeWarps = 12;
+constexpr int kTmaWarp = 12, kMmaWarp = 13;  // warps 14-17: epilogue
+constexpr int kGThreads = 32 * 18;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = GN;             // accumulator b at columns b * GN
 constexpr uint32_t kACol0 = 2 * GN;           // A stage d at columns kACol0 + 32 d
 static_assert(kACol0 + kDecStages * 32 <= kTmemCols, "TMEM holds both accumulators and the A stages");
 // Warp-tasks of one decoded stage: 32 rows x one half (32 elements) each.
-// A: 4 row quarters x 2 halves = 8; B: GN / 32 x 2 = 12.  Warp w takes tasks
-// w and w + kDecodeWarps; A task u (< 8) covers rows 32 (u % 4) .., which is
-// the TMEM lane quarter warp u may access (u % 4 == w % 4).
+// A: 4 row quarters x 2 halves = 8; B: GN / 32 x 2 = 12.  Decode warp w takes
+// B task w, and warps 0-7 also A task w, which covers rows 32 (w % 4) .. : the
+// TMEM lane quarter warp w may access.  (A's TMEM store costs less than B's
+// shared-memory store, so no warp holds two B tasks.)
 constexpr int kATasks = 8, kBTasks = 2 * GN / 32;
-static_assert(kATasks + kBTasks == 2 * kDecodeWarps, "two warp-tasks per decode warp");
+static_assert(kBTasks == kDecodeWarps && kATasks <= kDecodeWarps, "one B task per decode warp");
 static_assert(GKR / GKD == 4, "a raw stage is four decoded stages");
 
 struct Fp4GemmSmem {
@@ -110,11 +111,8 @@ struct DecTask {
   int row0;  // first of the 32 rows (within the operand's tile)
   int half;  // elements 32 half .. 32 half + 31 of each decoded stage
 };
-__device__ __forceinline__ DecTask dec_task(int u) {
-  if (u < kATasks) return {true, 32 * (u % 4), u / 4};
-  const int v = u - kATasks;
-  return {false, 32 * (v % (GN / 32)), v / (GN / 32)};
-}
+__device__ __forceinline__ DecTask a_task(int u) { return {true, 32 * (u % 4), u / 4}; }
+__device__ __forceinline__ DecTask b_task(int v) { return {false, 32 * (v % (GN / 32)), v / (GN / 32)}; }
 
 // Slot of 16-byte piece c (0..3) of staging row r: the layout of a 64-byte
 // swizzled box; 8 lanes writing piece c of 8 consecutive rows hit 8 bank groups.
@@ -198,7 +196,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // ------------------------------------------------------------ decode
     // Lanes take 32 consecutive rows, so the swizzled 16-byte loads and
     // stores of a quarter warp hit 8 distinct bank groups.
-    const DecTask tk[2] = {dec_task(warp), dec_task(warp + kDecodeWarps)};
+    // tk[0] is B task `warp`; warps 0-7 also hold A task `warp` as tk[1]
+    const int ntask = warp < kATasks ? 2 : 1;  // warp-uniform
+    const DecTask tk[2] = {b_task(warp), a_task(warp < kATasks ? warp : 0)};
     int rs = 0, ds = 0;  // raw / decoded stages passed (ring positions)
     bool ok = true;
     for (int tile = cta; tile < p.ntiles && ok; tile += ncta) {
@@ -214,7 +214,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int r = tk[i].row0 + lane;
-          sc[i] = *reinterpret_cast<const uint4*>(tk[i].is_a ? &sm.a_sc[s][r * 16] : &sm.b_sc[s][r * 16]);
+          sc[i] = make_uint4(0, 0, 0, 0);
+          if (i < ntask)
+            sc[i] = *reinterpret_cast<const uint4*>(tk[i].is_a ? &sm.a_sc[s][r * 16] : &sm.b_sc[s][r * 16]);
           cbase[i] = (tk[i].is_a ? sm.a_codes[s] : sm.b_codes[s]) + r * 128;
         }
         const int sw = lane & 7;  // (row & 7): the rows of a task start at multiples of 32
@@ -223,7 +225,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         uint4 nxt[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          nxt[i] = *reinterpret_cast<const uint4*>(cbase[i] + ((tk[i].half ^ sw) << 4));
+          nxt[i] = i < ntask ? *reinterpret_cast<const uint4*>(cbase[i] + ((tk[i].half ^ sw) << 4))
+                             : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
         for (int j = 0; j < GKR / GKD; ++j, ++ds) {
           const int d = ds % kDecStages;
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             codes[i] = nxt[i];
-            if (j + 1 < GKR / GKD)
+            if (i < ntask && j + 1 < GKR / GKD)
               nxt[i] = *reinterpret_cast<const uint4*>(cbase[i] + (((2 * (j + 1) + tk[i].half) ^ sw) << 4));
           }
           if (ds >= kDecStages && !mbar_wait(&sm.dec_empty[d], ((ds / kDecStages) - 1) & 1, wd)) {
@@ -240,6 +243,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           }
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
+            if (i >= ntask) break;
             const uint32_t scw = j == 0 ? sc[i].x : j == 1 ? sc[i].y : j == 2 ? sc[i].z : sc[i].w;
             uint32_t o[16];
             decode32(codes[i], scw >> (16 * tk[i].half), o);
