@@ -63,7 +63,7 @@ TRAFFIC = {
     # the FP4 attention with a staging buffer, one call: the decode pass and
     # the kernel (the bench times the call)
     "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>": {
-        "bytes": (32370688 + 52944896) + (314591232 + 26115328), "src_sha": "305a49bcf1322827"},
+        "bytes": (32370688 + 52944896) + (314591232 + 26115328), "src_sha": "e573755c624403a4"},
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
     "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
@@ -639,7 +639,7 @@ def main():
     kname = {"attn_bf16": "sinkwin_attn_kernel<128,false>",
              "attn_fp4": "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>",
              "recache": "recache_fused_kernel"}[dom]
-    src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_gemm_fp4.cu+kernels_attn.cu",
+    src = {"attn_bf16": "kernels_attn.cu", "attn_fp4": "kernels_decode.cu+kernels_attn.cu",
            "recache": "kernels_recache.cu"}[dom]
     tr = TRAFFIC.get(kname)
     traffic = tr["bytes"] if tr and tr["src_sha"] == _src_sha(src) else None

@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsinkwin.so")
 
 SOURCES = ["kvc_api.cu", "kernels_mem.cu", "kernels_attn.cu", "kernels_recache.cu",
-           "kernels_gemm_fp4.cu", "kvc_noalloc.cu"]
+           "kernels_gemm_fp4.cu", "kernels_decode.cu", "kvc_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
