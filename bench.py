@@ -59,11 +59,11 @@ TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum on the LongLive-1.3B
     # layer workload (one launch each); summary in
     # profiles/sinkwin_attn_layer1p3b_18720keys.md
-    "sinkwin_attn_kernel<128,false>": {"bytes": 310526976 + 26393344, "src_sha": "c76cdafbd9a1ff12"},
+    "sinkwin_attn_kernel<128,false>": {"bytes": 307172352 + 26303488, "src_sha": "c76cdafbd9a1ff12"},
     # the FP4 attention with a staging buffer, one call: the decode pass and
     # the kernel (the bench times the call)
     "fp4_to_f16_kernel + sinkwin_attn_kernel<128,true,true>": {
-        "bytes": (32370688 + 52944896) + (314591232 + 26115328), "src_sha": "e573755c624403a4"},
+        "bytes": (32358656 + 52979712) + (312098560 + 26046720), "src_sha": "3ec9106f5bcd859f"},
     # the fused recache: the cluster launch and the cluster-free launch beside
     # it (captured one after the other); summary in profiles/recache_gemm_layer1p3b.md
     "recache_fused_kernel": {"bytes": (67131392 + 60844800) + (16364544 + 10752), "src_sha": "a496e9122d019fca"},
@@ -317,6 +317,23 @@ def extra_rows(swl, dev, randn, wkv, wqkv, gamma, runs: int = 12):
                                    "what": f"bf16 attention, {tq} queries x 18720 keys x 12 heads; "
                                            "items spread over all SMs vs whole items per CTA"}
     del caches, whole
+    # the FP4 attention without a staging buffer (K/V decoded inside the
+    # kernel's tile load) next to the decode-once path the step uses
+    q = randn((TC, H, D), 1 / math.sqrt(D))
+    o = torch.empty_like(q)
+    flop = 4.0 * H * TC * LK * D
+    for name, st in (("attn_fp4_in_kernel_decode", False), ("attn_fp4_decode_once", True)):
+        cs = [filled("fp4", stage=st) for _ in range(2)]
+        ms = med(lambda i: cs[i % 2].attn(q, scale, out=o))
+        out[name] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+                     "what": "FP4-KV attention, 4680 queries x 18720 keys x 12 heads, "
+                             + ("K/V decoded in the kernel's tile load (no staging buffer)" if not st
+                                else "visible K/V decoded once into the staging buffer, then "
+                                     "f16 tiles by TMA")}
+        for c in cs:
+            if c.last_device_error() != swl.KVC_OK:
+                raise RuntimeError("device error in the FP4 attention rows")
+        del cs
     f4 = [filled("fp4", stage=True) for _ in range(2)]
     hid = randn((LK, HD))
     present = [0, 1, 2, 3]

@@ -41,6 +41,7 @@ __device__ __forceinline__ float inv_v_shift_of(const Fp4DecodeJobs& jj) {
 // kDecUnroll groups a pass, its loads issued before any use.  The f16 value is
 // e2m1(code) * e4m3(scale), exact; the tensor scale is applied by the consumer.
 __global__ void __launch_bounds__(kDecThreads) fp4_to_f16_kernel(const __grid_constant__ Fp4DecodeJobs jobs) {
+  pdl_launch_dependents();  // a dependent launched with PDL may set up meanwhile
   const Fp4DecodeJob& jb = jobs.j[blockIdx.y];
   const int64_t n = jb.groups;
   // tensor scale over G (jobs with a region): one fp32 rounding of the exact

@@ -416,6 +416,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      // launched as a programmatic dependent of the decode pass: everything
+      // above overlapped its tail; the f16 operands are complete from here on
+      // (every other access of this kernel follows these loads)
+      pdl_wait();
       int issued = 0;
       bool ok = true;
       for (int tile = cta; tile < p.ntiles && ok; tile += ncta) {
@@ -538,8 +542,17 @@ cudaError_t launch_gemm_fp4(const GemmFp4Launch& g, cudaStream_t st) {
     static bool done16[64] = {};
     e = set_smem_once(gemm_f16_kernel, smem, done16);
     if (e != cudaSuccess) return e;
-    gemm_f16_kernel<<<grid, kFThreads, smem, st>>>(tmA, tmB, tmC, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kFThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, p);
   }
 
   CUtensorMap tmAc, tmAs, tmBc, tmBs;
