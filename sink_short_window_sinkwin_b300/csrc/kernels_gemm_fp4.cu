@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // f16 GEMM fed by TMA.  The decode is done (M + N) K times instead of once per
 // tile, which on this GPU is worth the round trip through L2.
 // ---------------------------------------------------------------------------
-constexpr int kFStages = 4;
+constexpr int kFStages = 5;
 constexpr int kFThreads = 32 * 6;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 struct F16GemmSmem {
